@@ -1,0 +1,406 @@
+#!/usr/bin/env python3
+"""Throughput of one DCP causal MLA verify step on GB300.
+
+A step is the whole hot path for all dcp virtual ranks of one batch:
+metadata (row lengths, subpages, splits) -> split-KV partial attention ->
+LSE merge into the BF16 output. Inputs are seeded synthetic tensors resident
+in HBM; the default workload is the long-context one (batch 4, 128 heads,
+qlen 3, 1,048,576 tokens, dcp 8, FP8 cache), whose cache (2.4 GB) is far larger
+than L2, so no flush is needed between steps (smaller workloads flush L2 with a
+512 MB write before every timed step, outside the timed events).
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead (test infrastructure only).
+With ``--gpus N`` under torchrun every rank runs an independent replica of the
+workload (weak scaling; the dcp shards of a replica stay on its GPU).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV-tokens/s and TFLOP/s per verify step vs roofline fraction; μs per step"
+UNIT = "KV-tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic(w):
+    """Per-step KV tokens, flops and bytes (causal work only).
+
+    KV tokens = sum_b L_b (each token read once by its owner);
+    flops = sum_b sum_j H * g_j * 2 * (576 + 512);
+    bytes = sum_b L_b * 576 * elem + R*H*576*2 (q) + R*H*512*2 (out).
+    """
+    lens = [int(x) for x in w.seq_lens.cpu().tolist()]
+    H, qlen = w.num_heads, w.qlen
+    tokens = sum(lens)
+    flops = 0
+    for L in lens:
+        for j in range(qlen):
+            g = L - qlen + 1 + j if w.causal else L
+            flops += H * max(g, 0) * 2 * (576 + 512)
+    elem = 1 if w.kv_dtype == "fp8" else 2
+    R = w.batch * qlen
+    nbytes = tokens * 576 * elem + R * H * 576 * 2 + R * H * 512 * 2
+    return tokens, flops, nbytes
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index, path):
+        self.index, self.path, self.proc = index, path, None
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash():
+    import glob
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "decode_context_mla_causal_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM traffic per launch from the committed ncu summary, only if it was
+    taken on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}:{workload}")
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def oracle_prepare(w, b=0):
+    """Host copy of sequence b's blocks only (block table remapped)."""
+    import torch
+
+    import workloads
+
+    table = w.block_table[b].long()
+    sub = workloads.Workload(**{**w.__dict__})
+    sub.kv = w.kv[:, table].cpu()
+    sub.block_table = torch.arange(table.numel(), dtype=torch.int32).reshape(1, -1)
+    sub.seq_lens = w.seq_lens[b:b + 1].cpu()
+    sub.q = w.q[b * w.qlen:(b + 1) * w.qlen].cpu()
+    sub.batch, sub.num_blocks = 1, table.numel()
+    return dict(q_bits=sub.q_bits_np(), pools=sub.pools_np(),
+                block_table=sub.block_table.numpy(), seq_lens=sub.seq_lens.numpy(),
+                qlen=w.qlen, dcp=w.dcp, interleave=w.interleave, block_size=w.block_size,
+                kv_dtype=w.kv_dtype, kv_scale=w.kv_scale, softmax_scale=w.softmax_scale)
+
+
+def oracle_sample(w, prepared, heads_sample, rows_sample=None):
+    """Time the CPU oracle on sequence 0 for a subset of heads and rows."""
+    import oracle
+
+    heads = list(range(heads_sample))
+    rows = [(0, j) for j in range(w.qlen)] if rows_sample is None else rows_sample
+    t0 = time.perf_counter()
+    oracle.attention.forward(rows=rows, heads=heads, per_rank=False, **prepared)
+    dt = time.perf_counter() - t0
+    L = int(prepared["seq_lens"][0])
+    equiv_tokens = L * (len(heads) * len(rows)) / (w.num_heads * w.qlen)
+    return dict(value=equiv_tokens / dt, seconds=dt,
+                sample=(f"sequence 0 ({L} tokens), {len(rows)} of {w.qlen} verify rows, "
+                        f"{len(heads)} of {w.num_heads} heads; value = KV tokens x "
+                        f"(sampled rows*heads / all rows*heads) / seconds"))
+
+
+def oracle_cores():
+    try:
+        import numpy as np  # noqa: F401
+        return os.cpu_count()
+    except Exception:
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="c5", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-heads", type=int, default=0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import torch
+    import torch.distributed as dist
+
+    import workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import decode_context_mla_causal_gb300 as dm
+
+    w = workloads.generate(args.config, device=dev)
+    tokens, flops, nbytes = algorithmic(w)
+    ns = args.splits or dm.choose_num_splits(w.batch, w.qlen, w.num_heads, w.dcp,
+                                            w.max_local_len, w.block_size, dm.num_sms(dev))
+    dims = dm.make_dims(batch=w.batch, qlen=w.qlen, num_heads=w.num_heads, dcp=w.dcp,
+                        interleave=w.interleave, block_size=w.block_size,
+                        max_blocks_per_seq=w.max_blocks_per_seq, max_local_len=w.max_local_len,
+                        num_blocks=w.num_blocks, num_splits=ns)
+    kvt = dm.KV_FP8_E4M3 if w.kv_dtype == "fp8" else dm.KV_BF16
+    step = dm.VerifyStep(dims, kvt, dev)
+    scale = torch.tensor([w.kv_scale], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kv_bytes = w.kv.numel() * w.kv.element_size()
+    flush = None
+    if kv_bytes < 4 * 129 * 2**20:
+        flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=dev)
+
+    def run():
+        step.metadata(w.seq_lens, w.block_table)
+        step.partial(w.q, w.kv, scale, w.softmax_scale)
+        step.merge()
+
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    if step.read_status() != 0:
+        raise RuntimeError(f"device status {step.read_status():#x}")
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+                           if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
+                           else f"/tmp/dcp_clocks_{os.getpid()}.csv")
+    with sampler:
+        for i in range(K):
+            if flush is not None:
+                flush.fill_(float(i))
+            ev[i][0].record(stream)
+            step.metadata(w.seq_lens, w.block_table)
+            ev[i][1].record(stream)
+            step.partial(w.q, w.kv, scale, w.softmax_scale)
+            ev[i][2].record(stream)
+            step.merge()
+            ev[i][3].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = [ev[i][0].elapsed_time(ev[i][3]) for i in range(K)]
+    part_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    meta_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    merge_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
+    total_ms = sum(step_ms)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = tokens * world * K / (total_ms / 1e3)
+
+    # end to end through the C ABI with host buffers: per step H2D of q, seq_lens,
+    # block_table from pinned memory, the three calls, D2H of out and lse
+    hq = w.q.cpu().pin_memory()
+    hs = w.seq_lens.cpu().pin_memory()
+    ht = w.block_table.cpu().pin_memory()
+    ho = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    hl = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
+    dq, dsq, dt_ = torch.empty_like(w.q), torch.empty_like(w.seq_lens), torch.empty_like(w.block_table)
+    h2d = hq.numel() * hq.element_size() + hs.numel() * 4 + ht.numel() * 4
+    d2h = ho.numel() * ho.element_size() + hl.numel() * 4
+
+    def run_e2e():
+        dq.copy_(hq, non_blocking=True)
+        dsq.copy_(hs, non_blocking=True)
+        dt_.copy_(ht, non_blocking=True)
+        step.metadata(dsq, dt_)
+        step.partial(dq, w.kv, scale, w.softmax_scale)
+        step.merge()
+        ho.copy_(step.out, non_blocking=True)
+        hl.copy_(step.lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        run_e2e()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for i in range(K):
+        if flush is not None:
+            flush.fill_(float(i))
+        e0.record(stream)
+        run_e2e()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = tokens * world * K / (float(te.item()) / 1e3)
+
+    peaks, src = load_peaks()
+    part_avg = sum(part_ms) / K
+    achieved_tf = flops / (part_avg / 1e3) / 1e12
+    tensor_peak = float(peaks["bf16_tflops"])
+    hbm_peak = float(peaks["hbm_gbs"])
+    roof_ms = max(nbytes / (hbm_peak * 1e9), flops / (tensor_peak * 1e12)) * 1e3
+    clocks = sampler.summary()
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dm.COMPUTE_DTYPE,
+        "data": "synthetic (seeded N(0,1) q and cache, FP8 E4M3 per-tensor scale)",
+        "config": {"workload": f"{args.config} {workloads.DESCRIPTIONS[args.config]}",
+                   "global_batch": w.batch * world, "seq_len": int(w.seq_lens.max()),
+                   "qlen": w.qlen, "num_heads": w.num_heads, "dcp": w.dcp,
+                   "interleave": w.interleave, "num_splits": ns,
+                   "parallelism": f"dcp{w.dcp} virtual shards per GPU; replicas x{world}",
+                   "l2": ("flushed with a 512 MB write before each timed step" if flush is not None
+                          else f"inputs larger than L2 (cache {kv_bytes / 1e9:.2f} GB)")},
+        "us_per_step": ms_per_step * 1e3,
+        "tflops": flops / (ms_per_step / 1e3) / 1e12,
+        "kernel_us": {"metadata": 1e3 * sum(meta_ms) / K, "partial": 1e3 * part_avg,
+                      "merge": 1e3 * sum(merge_ms) / K},
+        "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": tensor_peak,
+                     "unit": "TFLOP/s", "frac": achieved_tf / tensor_peak,
+                     "traffic": profiled_traffic("partial", args.config),
+                     "peak_source": f"{src} bf16 dense (burst), MEASURED_PEAKS.json"
+                     if src == "measured" else "fallback 1.9 PFLOP/s bf16",
+                     "kernel": "dcp_mla_partial",
+                     "step_frac": roof_ms / ms_per_step,
+                     "hbm_bytes_algorithmic": nbytes,
+                     "hbm_frac_of_partial": nbytes / (part_avg / 1e3) / (hbm_peak * 1e9)},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        heads = args.oracle_heads or default_oracle_heads(args.config)
+        cb = oracle_sample(w, oracle_prepare(w), heads)
+        res["cpu_baseline"] = {"value": cb["value"], "unit": UNIT, "cores": oracle_cores(),
+                               "kind": "oracle", "sample": cb["sample"],
+                               "seconds": cb["seconds"]}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def default_oracle_heads(config):
+    return {"c1": 8, "c2": 96, "c3": 128, "c4": 128, "c5": 128}[config]
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    import torch
+
+    import workloads
+
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    w = workloads.generate(args.config, device=dev)
+    heads = args.oracle_heads or max(1, default_oracle_heads(args.config) // 4)
+    rows = [(0, w.qlen - 1)]
+    prepared = oracle_prepare(w)
+    oracle_sample(w, prepared, heads, rows)  # one untimed run (the oracle keeps no state)
+    vals, secs = [], 0.0
+    cb = None
+    for _ in range(args.steps):
+        cb = oracle_sample(w, prepared, heads, rows)
+        vals.append(cb["value"])
+        secs += cb["seconds"]
+    value = len(vals) / sum(1.0 / v for v in vals)
+    res = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "impl": "reference",
+           "config": {"workload": f"{args.config} {workloads.DESCRIPTIONS[args.config]}"},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_cores(),
+                            "kind": "oracle", "sample": cb["sample"]},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,22 @@
+"""DCP causal multi-token MLA verification attention for GB300 (sm_103a).
+
+The computation lives in ``libdcpmla.so`` (hand-written CUDA, C ABI declared in
+``include/dcp_mla.h``); this package is its thin Python binding. Importing the
+package loads the library and raises if it has not been built: there is no
+CPU or PyTorch fallback.
+"""
+
+from .binding import (  # noqa: F401
+    DCP_OK, DCP_ERR_INVALID_ARG, DCP_ERR_UNSUPPORTED, DCP_ERR_CUDA,
+    STATUS_BAD_SEQ_LEN, STATUS_LOCAL_OVER_BOUND, STATUS_BAD_BLOCK_ID, STATUS_BAD_PAGE,
+    STATUS_TIMEOUT, STATUS_BAD_SPLIT, KV_BF16, KV_FP8_E4M3, QK_DIM, V_DIM,
+    DcpError, Dims, load, library_path,
+    dcp_mla_subpage_size, dcp_mla_max_pages, dcp_mla_check_dims,
+    dcp_mla_metadata, dcp_mla_partial, dcp_lse_merge, dcp_last_error,
+)
+from .step import VerifyStep, choose_num_splits, make_dims, num_sms  # noqa: F401
+
+#: Arithmetic type of the hot path (reported by bench.py).
+COMPUTE_DTYPE = "f32"
+
+load()

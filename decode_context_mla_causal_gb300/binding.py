@@ -1,0 +1,201 @@
+"""ctypes binding of libdcpmla.so (argument marshalling only).
+
+Each function has the name of the C entry point it calls and takes torch
+tensors in place of raw pointers; it checks dtype, device, contiguity and size,
+passes ``data_ptr()`` and the current CUDA stream, and raises ``DcpError`` on a
+non-OK return. Every step of the computation runs in the library's kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+QK_DIM = 576
+V_DIM = 512
+
+DCP_OK = 0
+DCP_ERR_INVALID_ARG = 1
+DCP_ERR_UNSUPPORTED = 2
+DCP_ERR_CUDA = 3
+
+STATUS_BAD_SEQ_LEN = 0x1
+STATUS_LOCAL_OVER_BOUND = 0x2
+STATUS_BAD_BLOCK_ID = 0x4
+STATUS_BAD_PAGE = 0x8
+STATUS_TIMEOUT = 0x10
+STATUS_BAD_SPLIT = 0x20
+
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+
+
+class DcpError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"dcp status {code}: {msg}")
+        self.code = code
+
+
+class Dims(ctypes.Structure):
+    """Mirror of ``dcp_mla_dims`` (include/dcp_mla.h)."""
+
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "qlen", "num_heads", "dcp", "interleave", "block_size",
+        "max_blocks_per_seq", "max_local_len", "num_blocks", "num_splits", "causal")]
+
+    def __repr__(self):
+        return "Dims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
+
+    @property
+    def rows(self) -> int:
+        return self.batch * self.qlen
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libdcpmla.so; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it with __graft_entry__.build() or "
+            "python decode_context_mla_causal_gb300/build.py (there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    I = ctypes.c_int32
+    D = ctypes.POINTER(Dims)
+    sig = {
+        "dcp_mla_subpage_size": (I, [I]),
+        "dcp_mla_max_pages": (I, [D]),
+        "dcp_mla_check_dims": (I, [D, I, I]),
+        "dcp_mla_metadata": (I, [D, P, P, I, I, P, P, P, P, P, P]),
+        "dcp_mla_partial": (I, [D, P, P, I, P, ctypes.c_float, I, I, P, P, P, P, P, P, P, P, P]),
+        "dcp_lse_merge": (I, [D, I, P, P, P, P, P, P, P, P]),
+        "dcp_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def dcp_last_error() -> str:
+    return load().dcp_last_error().decode()
+
+
+def _check(code: int):
+    if code != DCP_OK:
+        raise DcpError(code, dcp_last_error())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t, dtype, numel, name, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} has {t.numel()} elements, needs {numel}")
+    return t.data_ptr()
+
+
+def dcp_mla_subpage_size(block_size: int) -> int:
+    return load().dcp_mla_subpage_size(block_size)
+
+
+def dcp_mla_max_pages(dims: Dims) -> int:
+    return load().dcp_mla_max_pages(ctypes.byref(dims))
+
+
+def dcp_mla_check_dims(dims: Dims, rank_begin: int = 0, num_ranks: int | None = None):
+    nr = dims.dcp - rank_begin if num_ranks is None else num_ranks
+    _check(load().dcp_mla_check_dims(ctypes.byref(dims), rank_begin, nr))
+
+
+def dcp_mla_metadata(dims, seq_lens, block_table, rank_begin, num_ranks, row_len, page_ids,
+                     split_beg, split_end, status, stream=None):
+    lib = load()
+    B, R, NS = dims.batch, dims.rows, dims.num_splits
+    MP = lib.dcp_mla_max_pages(ctypes.byref(dims))
+    if MP < 0:
+        _check(lib.dcp_mla_check_dims(ctypes.byref(dims), rank_begin, num_ranks))
+    i32 = torch.int32
+    _check(lib.dcp_mla_metadata(
+        ctypes.byref(dims), _ptr(seq_lens, i32, B, "seq_lens"),
+        _ptr(block_table, i32, B * dims.max_blocks_per_seq, "block_table"),
+        rank_begin, num_ranks,
+        _ptr(row_len, i32, num_ranks * R, "row_len"),
+        _ptr(page_ids, i32, num_ranks * B * MP, "page_ids"),
+        _ptr(split_beg, i32, num_ranks * B * NS, "split_beg"),
+        _ptr(split_end, i32, num_ranks * B * NS, "split_end"),
+        _ptr(status, i32, 1, "status"), _stream(stream)))
+
+
+def dcp_mla_partial(dims, q, kv, kv_dtype, kv_scale, softmax_scale, rank_begin, num_ranks,
+                    row_len, page_ids, split_beg, split_end, part_o, part_m, part_l, status,
+                    stream=None):
+    lib = load()
+    B, R, H, NS = dims.batch, dims.rows, dims.num_heads, dims.num_splits
+    MP = lib.dcp_mla_max_pages(ctypes.byref(dims))
+    i32 = torch.int32
+    f32 = torch.float32
+    kv_elem = torch.uint8 if kv_dtype == KV_FP8_E4M3 else torch.bfloat16
+    pool = dims.num_blocks * dims.block_size * QK_DIM
+    _check(lib.dcp_mla_partial(
+        ctypes.byref(dims), _ptr(q, torch.bfloat16, R * H * QK_DIM, "q"),
+        _ptr(kv, kv_elem, num_ranks * pool, "kv"), int(kv_dtype),
+        _ptr(kv_scale, f32, 1, "kv_scale", allow_none=True), float(softmax_scale),
+        rank_begin, num_ranks,
+        _ptr(row_len, i32, num_ranks * R, "row_len"),
+        _ptr(page_ids, i32, num_ranks * B * max(MP, 0), "page_ids"),
+        _ptr(split_beg, i32, num_ranks * B * NS, "split_beg"),
+        _ptr(split_end, i32, num_ranks * B * NS, "split_end"),
+        _ptr(part_o, f32, num_ranks * NS * R * H * V_DIM, "part_o"),
+        _ptr(part_m, f32, num_ranks * NS * R * H, "part_m"),
+        _ptr(part_l, f32, num_ranks * NS * R * H, "part_l"),
+        _ptr(status, i32, 1, "status"), _stream(stream)))
+
+
+def dcp_lse_merge(dims, num_ranks, part_o, part_m, part_l, out, lse, rank_lse=None,
+                  status=None, stream=None):
+    lib = load()
+    R, H, NS = dims.rows, dims.num_heads, dims.num_splits
+    f32 = torch.float32
+    _check(lib.dcp_lse_merge(
+        ctypes.byref(dims), num_ranks,
+        _ptr(part_o, f32, num_ranks * NS * R * H * V_DIM, "part_o"),
+        _ptr(part_m, f32, num_ranks * NS * R * H, "part_m"),
+        _ptr(part_l, f32, num_ranks * NS * R * H, "part_l"),
+        _ptr(out, torch.bfloat16, R * H * V_DIM, "out"),
+        _ptr(lse, f32, R * H, "lse"),
+        _ptr(rank_lse, f32, num_ranks * R * H, "rank_lse", allow_none=True),
+        _ptr(status, torch.int32, 1, "status"), _stream(stream)))

@@ -1,0 +1,157 @@
+// C ABI entry points: argument validation, error reporting, launches.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "common.cuh"
+
+namespace dcpmla {
+
+static thread_local std::string g_last_error;
+
+dcp_status fail(dcp_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+static int32_t subpage_of(int32_t block_size) {
+  if (block_size <= 0) return -1;
+  int32_t low = block_size & (-block_size);
+  return low < 128 ? low : 128;
+}
+
+Derived derive(const dcp_mla_dims& d) {
+  Derived x;
+  x.rows = d.batch * d.qlen;
+  x.subpage = subpage_of(d.block_size);
+  x.ppb = d.block_size / x.subpage;
+  x.max_pages = (d.max_local_len + x.subpage - 1) / x.subpage;
+  return x;
+}
+
+static dcp_status check(const dcp_mla_dims* d, int32_t rank_begin, int32_t num_ranks) {
+  g_last_error.clear();
+  if (d == nullptr) return fail(DCP_ERR_INVALID_ARG, "dims is NULL");
+  if (d->batch < 0) return fail(DCP_ERR_INVALID_ARG, "batch must be >= 0 (got %d)", d->batch);
+  if (d->qlen < 1) return fail(DCP_ERR_INVALID_ARG, "qlen must be >= 1 (got %d)", d->qlen);
+  if (d->num_heads < 1 || d->num_heads > 1024)
+    return fail(DCP_ERR_INVALID_ARG, "num_heads must be in [1, 1024] (got %d)", d->num_heads);
+  if (d->dcp < 1) return fail(DCP_ERR_INVALID_ARG, "dcp must be >= 1 (got %d)", d->dcp);
+  if (d->block_size < 1)
+    return fail(DCP_ERR_INVALID_ARG, "block_size must be >= 1 (got %d)", d->block_size);
+  if (d->interleave < 1 || d->interleave > d->block_size)
+    return fail(DCP_ERR_INVALID_ARG, "interleave must be in [1, block_size] (got %d)",
+                d->interleave);
+  if (d->interleave > 1 && d->block_size % d->interleave != 0)
+    return fail(DCP_ERR_INVALID_ARG, "block_size %% interleave must be 0 when interleave > 1");
+  if (d->max_local_len < 0)
+    return fail(DCP_ERR_INVALID_ARG, "max_local_len must be >= 0 (got %d)", d->max_local_len);
+  if (d->max_blocks_per_seq < 1)
+    return fail(DCP_ERR_INVALID_ARG, "max_blocks_per_seq must be >= 1");
+  if ((int64_t)d->max_blocks_per_seq * d->block_size < (int64_t)d->max_local_len)
+    return fail(DCP_ERR_INVALID_ARG,
+                "max_blocks_per_seq * block_size (%lld) must cover max_local_len (%d)",
+                (long long)d->max_blocks_per_seq * d->block_size, d->max_local_len);
+  if (d->num_blocks < 1) return fail(DCP_ERR_INVALID_ARG, "num_blocks must be >= 1");
+  if ((int64_t)d->num_blocks * d->block_size > (int64_t)INT32_MAX)
+    return fail(DCP_ERR_UNSUPPORTED, "num_blocks * block_size must fit in int32");
+  if (d->num_splits < 1 || d->num_splits > 4096)
+    return fail(DCP_ERR_INVALID_ARG, "num_splits must be in [1, 4096] (got %d)", d->num_splits);
+  if (d->causal != 0 && d->causal != 1)
+    return fail(DCP_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if ((int64_t)d->batch * d->qlen * d->num_heads > (int64_t)(1 << 24))
+    return fail(DCP_ERR_UNSUPPORTED, "batch*qlen*num_heads above 2^24");
+  if (rank_begin < 0 || num_ranks < 1 || (int64_t)rank_begin + num_ranks > d->dcp)
+    return fail(DCP_ERR_INVALID_ARG, "rank range [%d, %d) outside [0, dcp=%d)", rank_begin,
+                rank_begin + num_ranks, d->dcp);
+  return DCP_OK;
+}
+
+static dcp_status launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess)
+    return fail(DCP_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
+  return DCP_OK;
+}
+
+}  // namespace dcpmla
+
+using namespace dcpmla;
+
+extern "C" {
+
+int32_t dcp_mla_subpage_size(int32_t block_size) { return subpage_of(block_size); }
+
+int32_t dcp_mla_max_pages(const dcp_mla_dims* dims) {
+  if (check(dims, 0, dims ? (dims->dcp > 0 ? dims->dcp : 1) : 1) != DCP_OK) return -1;
+  return derive(*dims).max_pages;
+}
+
+dcp_status dcp_mla_check_dims(const dcp_mla_dims* dims, int32_t rank_begin, int32_t num_ranks) {
+  return check(dims, rank_begin, num_ranks);
+}
+
+dcp_status dcp_mla_metadata(const dcp_mla_dims* dims, const int32_t* seq_lens,
+                            const int32_t* block_table, int32_t rank_begin, int32_t num_ranks,
+                            int32_t* row_len, int32_t* page_ids, int32_t* split_beg,
+                            int32_t* split_end, uint32_t* status, dcp_stream_t stream) {
+  dcp_status s = check(dims, rank_begin, num_ranks);
+  if (s != DCP_OK) return s;
+  if (dims->batch == 0) return DCP_OK;
+  if (!seq_lens || !block_table || !row_len || !page_ids || !split_beg || !split_end || !status)
+    return fail(DCP_ERR_INVALID_ARG, "dcp_mla_metadata: a required pointer is NULL");
+  Derived x = derive(*dims);
+  return launched(launch_metadata(*dims, x, seq_lens, block_table, rank_begin, num_ranks,
+                                  row_len, page_ids, split_beg, split_end, status,
+                                  (cudaStream_t)stream),
+                  "dcp_mla_metadata");
+}
+
+dcp_status dcp_mla_partial(const dcp_mla_dims* dims, const void* q, const void* kv,
+                           dcp_kv_dtype kv_dtype, const float* kv_scale, float softmax_scale,
+                           int32_t rank_begin, int32_t num_ranks, const int32_t* row_len,
+                           const int32_t* page_ids, const int32_t* split_beg,
+                           const int32_t* split_end, float* part_o, float* part_m,
+                           float* part_l, uint32_t* status, dcp_stream_t stream) {
+  dcp_status s = check(dims, rank_begin, num_ranks);
+  if (s != DCP_OK) return s;
+  if (kv_dtype != DCP_KV_BF16 && kv_dtype != DCP_KV_FP8_E4M3)
+    return fail(DCP_ERR_INVALID_ARG, "unknown kv_dtype %d", (int)kv_dtype);
+  if (!(softmax_scale > 0.0f) || softmax_scale > 1e30f)
+    return fail(DCP_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+  if (dims->batch == 0) return DCP_OK;
+  if (!q || !kv || !row_len || !page_ids || !split_beg || !split_end || !part_o || !part_m ||
+      !part_l || !status)
+    return fail(DCP_ERR_INVALID_ARG, "dcp_mla_partial: a required pointer is NULL");
+  if (((uintptr_t)q & 15) || ((uintptr_t)kv & 15) || ((uintptr_t)part_o & 15))
+    return fail(DCP_ERR_INVALID_ARG, "q, kv and part_o must be 16-byte aligned");
+  Derived x = derive(*dims);
+  return launched(launch_partial(*dims, x, q, kv, kv_dtype, kv_scale, softmax_scale, num_ranks,
+                                 row_len, page_ids, split_beg, split_end, part_o, part_m, part_l,
+                                 status, (cudaStream_t)stream),
+                  "dcp_mla_partial");
+}
+
+dcp_status dcp_lse_merge(const dcp_mla_dims* dims, int32_t num_ranks, const float* part_o,
+                         const float* part_m, const float* part_l, void* out, float* lse,
+                         float* rank_lse, uint32_t* status, dcp_stream_t stream) {
+  dcp_status s = check(dims, 0, num_ranks);
+  if (s != DCP_OK) return s;
+  if (dims->batch == 0) return DCP_OK;
+  if (!part_o || !part_m || !part_l || !out || !lse || !status)
+    return fail(DCP_ERR_INVALID_ARG, "dcp_lse_merge: a required pointer is NULL");
+  if (((uintptr_t)part_o & 15) || ((uintptr_t)out & 7))
+    return fail(DCP_ERR_INVALID_ARG, "part_o must be 16-byte and out 8-byte aligned");
+  Derived x = derive(*dims);
+  return launched(launch_merge(*dims, x, num_ranks, part_o, part_m, part_l, out, lse, rank_lse,
+                               status, (cudaStream_t)stream),
+                  "dcp_lse_merge");
+}
+
+const char* dcp_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

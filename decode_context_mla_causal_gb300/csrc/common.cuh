@@ -1,0 +1,49 @@
+// Shared definitions of the CUDA library (not shared with the CPU oracle).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dcp_mla.h"
+
+namespace dcpmla {
+
+constexpr int kDqk = DCP_MLA_QK_DIM;  // 576
+constexpr int kDv = DCP_MLA_V_DIM;    // 512
+
+// Host-side derived sizes of a dims struct (validated by check_dims first).
+struct Derived {
+  int rows;       // R = batch * qlen
+  int subpage;    // P
+  int ppb;        // subpages per block
+  int max_pages;  // MP
+};
+
+Derived derive(const dcp_mla_dims& d);
+
+// Record a message for dcp_last_error() and return the status.
+dcp_status fail(dcp_status s, const char* fmt, ...);
+
+// Internal launchers (argument checks already done by the API layer).
+cudaError_t launch_metadata(const dcp_mla_dims& d, const Derived& x, const int32_t* seq_lens,
+                            const int32_t* block_table, int rank_begin, int num_ranks,
+                            int32_t* row_len, int32_t* page_ids, int32_t* split_beg,
+                            int32_t* split_end, uint32_t* status, cudaStream_t stream);
+
+cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* q,
+                           const void* kv, dcp_kv_dtype kv_dtype, const float* kv_scale,
+                           float softmax_scale, int num_ranks, const int32_t* row_len,
+                           const int32_t* page_ids, const int32_t* split_beg,
+                           const int32_t* split_end, float* part_o, float* part_m,
+                           float* part_l, uint32_t* status, cudaStream_t stream);
+
+cudaError_t launch_merge(const dcp_mla_dims& d, const Derived& x, int num_ranks,
+                         const float* part_o, const float* part_m, const float* part_l,
+                         void* out, float* lse, float* rank_lse, uint32_t* status,
+                         cudaStream_t stream);
+
+__device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bits) {
+  if (status != nullptr) atomicOr(status, bits);
+}
+
+}  // namespace dcpmla

@@ -1,0 +1,89 @@
+"""One verify step (metadata -> partial -> merge) over preallocated buffers.
+
+Host-side plumbing around the three C entry points: it sizes and allocates the
+device buffers once (torch tensors), then every call launches the three
+kernels on one stream with no host synchronisation, so a call can be captured
+in a CUDA graph and replayed with new ``seq_lens`` / ``block_table`` / ``q``
+contents up to the static bound.
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import binding as B
+
+
+def num_sms(device=None) -> int:
+    return torch.cuda.get_device_properties(device or torch.cuda.current_device()).multi_processor_count
+
+
+def choose_num_splits(batch: int, qlen: int, num_heads: int, num_ranks: int,
+                      max_local_len: int, block_size: int, sms: int = 152) -> int:
+    """Static split count: enough CTAs to fill every SM twice over, while each
+    split keeps at least four subpages of work at the static bound."""
+    P = B.dcp_mla_subpage_size(block_size)
+    pages = max(1, math.ceil(max_local_len / P))
+    tiles = math.ceil(qlen * num_heads / 128)
+    ctas = max(1, batch * num_ranks * tiles)
+    want = max(1, math.ceil(2 * sms / ctas))
+    return int(max(1, min(want, pages // 4 if pages >= 4 else 1, 256)))
+
+
+def make_dims(*, batch, qlen, num_heads, dcp, interleave, block_size, max_blocks_per_seq,
+              max_local_len, num_blocks, num_splits, causal=True) -> B.Dims:
+    return B.Dims(batch, qlen, num_heads, dcp, interleave, block_size, max_blocks_per_seq,
+                  max_local_len, num_blocks, num_splits, 1 if causal else 0)
+
+
+class VerifyStep:
+    """Buffers + launches for ranks ``[rank_begin, rank_begin + num_ranks)``."""
+
+    def __init__(self, dims: B.Dims, kv_dtype: int, device=None, rank_begin: int = 0,
+                 num_ranks: int | None = None, rank_lse: bool = True):
+        B.dcp_mla_check_dims(dims, rank_begin, num_ranks)
+        self.dims = dims
+        self.kv_dtype = kv_dtype
+        self.rank_begin = rank_begin
+        self.num_ranks = dims.dcp - rank_begin if num_ranks is None else num_ranks
+        dev = torch.device(device or "cuda")
+        nr, Bt, R, H, NS = self.num_ranks, dims.batch, dims.rows, dims.num_heads, dims.num_splits
+        MP = B.dcp_mla_max_pages(dims)
+        i32, f32 = torch.int32, torch.float32
+        self.row_len = torch.empty((nr, R), dtype=i32, device=dev)
+        self.page_ids = torch.empty((nr, Bt, MP), dtype=i32, device=dev)
+        self.split_beg = torch.empty((nr, Bt, NS), dtype=i32, device=dev)
+        self.split_end = torch.empty((nr, Bt, NS), dtype=i32, device=dev)
+        self.part_o = torch.empty((nr, NS, R, H, B.V_DIM), dtype=f32, device=dev)
+        self.part_m = torch.empty((nr, NS, R, H), dtype=f32, device=dev)
+        self.part_l = torch.empty((nr, NS, R, H), dtype=f32, device=dev)
+        self.out = torch.empty((R, H, B.V_DIM), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((R, H), dtype=f32, device=dev)
+        self.rank_lse = torch.empty((nr, R, H), dtype=f32, device=dev) if rank_lse else None
+        self.status = torch.zeros(1, dtype=i32, device=dev)
+
+    def metadata(self, seq_lens, block_table, stream=None):
+        B.dcp_mla_metadata(self.dims, seq_lens, block_table, self.rank_begin, self.num_ranks,
+                           self.row_len, self.page_ids, self.split_beg, self.split_end,
+                           self.status, stream)
+
+    def partial(self, q, kv, kv_scale, softmax_scale, stream=None):
+        B.dcp_mla_partial(self.dims, q, kv, self.kv_dtype, kv_scale, softmax_scale,
+                          self.rank_begin, self.num_ranks, self.row_len, self.page_ids,
+                          self.split_beg, self.split_end, self.part_o, self.part_m,
+                          self.part_l, self.status, stream)
+
+    def merge(self, stream=None):
+        B.dcp_lse_merge(self.dims, self.num_ranks, self.part_o, self.part_m, self.part_l,
+                        self.out, self.lse, self.rank_lse, self.status, stream)
+
+    def __call__(self, q, kv, kv_scale, softmax_scale, seq_lens, block_table, stream=None):
+        self.metadata(seq_lens, block_table, stream)
+        self.partial(q, kv, kv_scale, softmax_scale, stream)
+        self.merge(stream)
+        return self.out, self.lse
+
+    def read_status(self) -> int:
+        return int(self.status.item()) & 0xFFFFFFFF

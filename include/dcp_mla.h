@@ -1,0 +1,208 @@
+/*
+ * dcp_mla.h -- C ABI of libdcpmla.so: decode-context-parallel (DCP) causal
+ * multi-token MLA verification attention over a paged latent KV cache, for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method (sources are named by page title and section):
+ *
+ *   "Context Parallel Guide (PCP & DCP)" -- Decode Context Parallel (DCP) Guide.
+ *     The latent KV cache is sharded by sequence position over `dcp` ranks:
+ *     token p lives on rank (p / S) % dcp (S = interleave_size), at rank-local
+ *     index (p / (S*dcp))*S + p % S ("--dcp-config" table, "interleave_size").
+ *     One block-table entry is shared by all ranks and names, on each rank, that
+ *     rank's own physical block of block_size local tokens ("How it works" 1).
+ *     Each rank attends its local KV and returns its LSE; the partial outputs are
+ *     LSE-corrected and summed ("Decode"). FP8 caches use one per-tensor scale.
+ *   "Support Kimi-K3 DCP with DSpark" -- review thread: the rank-local length of
+ *     a row with global boundary g is
+ *       g/(dcp*S)*S + clamp(g % (dcp*S) - rank*S, 0, S).
+ *   "[ROCm][MLA][DCP] Support causal multi-token verification" -- Implementation:
+ *     (1) each verification row's global causal boundary is mapped to its
+ *     rank-local KV length; (2) physical blocks are expanded into bounded
+ *     subpages; (3) split-KV MLA emits unreduced partial outputs with base-2
+ *     max/sum statistics, later turned into natural-log LSE; (4) an LSE merge
+ *     produces the BF16 output. Row metadata is laid out at a static maximum
+ *     local bound so that the launches can be captured in a CUDA graph.
+ *
+ * Readings this library takes where the pages are silent:
+ *   - seq_lens[b] counts every token of sequence b INCLUDING its qlen verify
+ *     tokens, whose latent rows are already in the cache; verify row j (0-based)
+ *     attends global positions [0, g_j) with g_j = seq_lens[b] - qlen + 1 + j.
+ *     With dims.causal == 0 every row attends [0, seq_lens[b]) (the
+ *     bidirectional DSpark draft block of "DCP + Speculative Decode").
+ *   - Absorbed MLA: q and k are 576 wide (512 latent + 64 rope); v is the first
+ *     512 dims of the same cache row.
+ *   - Subpage size P = min(128, largest power of two dividing block_size);
+ *     subpage p of a sequence (p < ceil(local_len / P)) is numbered
+ *     block_table[b][p / ppb] * ppb + p % ppb (ppb = block_size / P) and covers
+ *     rows [page*P, page*P + P) of a rank's flat pool [num_blocks*block_size][576].
+ *   - Split s of num_splits covers subpages [s*np/NS, (s+1)*np/NS) (floor) of
+ *     the np subpages the longest row of the sequence needs on that rank.
+ *
+ * Conventions shared by every call:
+ *   - Every pointer argument named as device memory must point to device memory
+ *     of the current device; the caller allocates and frees all buffers. The
+ *     library never allocates, frees, synchronises, or reads device data on the
+ *     host, so every call may be captured in a CUDA graph.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - Ranks: a call handles ranks [rank_begin, rank_begin + num_ranks) of the
+ *     dcp group. One rank per call is the per-device form; all dcp ranks in one
+ *     call run them as virtual shards of one device's memory.
+ *   - Return value: host-checkable argument errors return DCP_ERR_INVALID_ARG or
+ *     DCP_ERR_UNSUPPORTED before anything is launched; a failed launch returns
+ *     DCP_ERR_CUDA. dcp_last_error() then holds a message (thread-local).
+ *   - Data errors found on the device never trap: the kernel ORs a
+ *     DCP_STATUS_* bit into *status (a device word the caller zeroes), masks the
+ *     offending work and carries on.
+ *   - All integers are int32 unless stated; all arrays are dense, row-major,
+ *     with the shapes given ("nr" = num_ranks, R = batch*qlen, H = num_heads,
+ *     MP = dcp_mla_max_pages(dims), NS = num_splits, MB = max_blocks_per_seq).
+ */
+#ifndef DCP_MLA_H
+#define DCP_MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DCP_MLA_QK_DIM 576 /* q/k width: 512 latent + 64 rope */
+#define DCP_MLA_V_DIM 512  /* v width: the latent part of the same cache row */
+
+struct CUstream_st;
+typedef struct CUstream_st* dcp_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  DCP_OK = 0,
+  DCP_ERR_INVALID_ARG = 1, /* a size, pointer or rank range is invalid     */
+  DCP_ERR_UNSUPPORTED = 2, /* valid, but outside what the kernels support  */
+  DCP_ERR_CUDA = 3         /* a CUDA launch or runtime call failed         */
+} dcp_status;
+
+/* Bits ORed into the device status word. */
+#define DCP_STATUS_BAD_SEQ_LEN 0x1u     /* seq_len < 0, or < qlen when causal     */
+#define DCP_STATUS_LOCAL_OVER_BOUND 0x2u /* local length > max_local_len (clamped) */
+#define DCP_STATUS_BAD_BLOCK_ID 0x4u    /* block id outside [0, num_blocks)        */
+#define DCP_STATUS_BAD_PAGE 0x8u        /* partial kernel met an invalid page id   */
+#define DCP_STATUS_TIMEOUT 0x10u        /* an on-device wait gave up (bounded)     */
+#define DCP_STATUS_BAD_SPLIT 0x20u      /* split bounds outside [0, MP]            */
+
+typedef enum { DCP_KV_BF16 = 0, DCP_KV_FP8_E4M3 = 1 } dcp_kv_dtype;
+
+/* Static problem description (host memory, read during the call only). For a
+ * captured graph every field is fixed; the data that varies between replays
+ * (seq_lens, block_table, q, kv) lives in device buffers. */
+typedef struct {
+  int32_t batch;              /* B sequences, >= 0 (0: every call is a no-op)  */
+  int32_t qlen;               /* verify rows per sequence, >= 1                */
+  int32_t num_heads;          /* H query heads, 1..1024                        */
+  int32_t dcp;                /* W ranks in the dcp group, >= 1                */
+  int32_t interleave;         /* S, 1 <= S <= block_size, block_size % S == 0  */
+  int32_t block_size;         /* tokens per physical block on each rank        */
+  int32_t max_blocks_per_seq; /* MB, block_table row stride; MB*block_size must
+                                 be >= max_local_len                           */
+  int32_t max_local_len;      /* static bound on every rank-local length       */
+  int32_t num_blocks;         /* NB, blocks in each rank's pool                */
+  int32_t num_splits;         /* NS, static split count per (rank, sequence)   */
+  int32_t causal;             /* 1: per-row causal boundary; 0: whole sequence */
+} dcp_mla_dims;
+
+/* Subpage size for a block size: min(128, largest power of two dividing it),
+ * or -1 if block_size <= 0. ("[ROCm][MLA][DCP] Support causal multi-token
+ * verification", Implementation item 2 and the review on the subpage bound.) */
+int32_t dcp_mla_subpage_size(int32_t block_size);
+
+/* MP = ceil(max_local_len / subpage), the page-table row length at the static
+ * bound; -1 if the dims are invalid. */
+int32_t dcp_mla_max_pages(const dcp_mla_dims* dims);
+
+/* Validate dims and a rank range without launching anything. */
+dcp_status dcp_mla_check_dims(const dcp_mla_dims* dims, int32_t rank_begin, int32_t num_ranks);
+
+/*
+ * Step 1+2: per-row rank-local lengths, subpages and split bounds.
+ * Defined by: "Support Kimi-K3 DCP with DSpark" (review: local length formula);
+ * "[ROCm][MLA][DCP] Support causal multi-token verification" (Implementation
+ * items 1, 2 and 5); "Context Parallel Guide (PCP & DCP)" ("How it works" 1).
+ *
+ *   seq_lens    device int32 [B]           global lengths (incl. verify tokens)
+ *   block_table device int32 [B][MB]       shared block ids; entries past the
+ *                                          ones a sequence needs are not read
+ *   row_len     device int32 [nr][R]       out: rank-local length of each row
+ *                                          (row = b*qlen + j), clamped to
+ *                                          max_local_len
+ *   page_ids    device int32 [nr][B][MP]   out: subpage ids, -1 past the last
+ *                                          needed subpage or for a bad block id
+ *   split_beg,  device int32 [nr][B][NS]   out: subpage range of each split
+ *   split_end
+ *   status      device uint32 [1]          in/out: DCP_STATUS_BAD_SEQ_LEN,
+ *                                          _LOCAL_OVER_BOUND, _BAD_BLOCK_ID ORed
+ * Every output element is written (bit-exact, padding included).
+ */
+dcp_status dcp_mla_metadata(const dcp_mla_dims* dims, const int32_t* seq_lens,
+                            const int32_t* block_table, int32_t rank_begin, int32_t num_ranks,
+                            int32_t* row_len, int32_t* page_ids, int32_t* split_beg,
+                            int32_t* split_end, uint32_t* status, dcp_stream_t stream);
+
+/*
+ * Step 3: split-KV absorbed-MLA partial attention on each rank's local KV.
+ * Defined by: "[ROCm][MLA][DCP] Support causal multi-token verification",
+ * Implementation item 3 (unreduced partial outputs with base-2 statistics);
+ * "Context Parallel Guide (PCP & DCP)", "Decode" (each rank attends its 1/dcp
+ * of the KV) and "How it works" 4 (FP8 with a per-tensor scale).
+ *
+ *   q           device bf16 [R][H][576]     query rows (row = b*qlen + j)
+ *   kv          device [nr][NB][block_size][576], E4M3 codes (uint8) or bf16;
+ *               the pool of rank rank_begin+k starts at element k*NB*bs*576
+ *   kv_scale    device float [1]: per-tensor dequantisation scale (NULL = 1)
+ *   softmax_scale  multiplies q.k (e.g. 1/sqrt(192))
+ *   row_len, page_ids, split_beg, split_end: dcp_mla_metadata's outputs for the
+ *               same dims and ranks
+ *   part_o      device float [nr][NS][R][H][512]  out: per-split normalised
+ *               output sum_t 2^(s_t - m) v_t / l   (0 for an empty split)
+ *   part_m      device float [nr][NS][R][H]  out: m = max_t s_t, where
+ *               s_t = softmax_scale * kv_scale * log2(e) * (q . k_t) (base 2);
+ *               -inf for an empty split
+ *   part_l      device float [nr][NS][R][H]  out: l = sum_t 2^(s_t - m)
+ *   status      device uint32 [1]            in/out: DCP_STATUS_BAD_PAGE,
+ *               DCP_STATUS_BAD_SPLIT, DCP_STATUS_TIMEOUT
+ * Tokens at or beyond a row's length, and pages with invalid ids, never reach
+ * the result (invalid ids also set DCP_STATUS_BAD_PAGE).
+ */
+dcp_status dcp_mla_partial(const dcp_mla_dims* dims, const void* q, const void* kv,
+                           dcp_kv_dtype kv_dtype, const float* kv_scale, float softmax_scale,
+                           int32_t rank_begin, int32_t num_ranks, const int32_t* row_len,
+                           const int32_t* page_ids, const int32_t* split_beg,
+                           const int32_t* split_end, float* part_o, float* part_m,
+                           float* part_l, uint32_t* status, dcp_stream_t stream);
+
+/*
+ * Step 4: LSE merge of all splits of all ranks into the BF16 output.
+ * Defined by: "Context Parallel Guide (PCP & DCP)", "Decode" (LSE-correct and
+ * reduce the per-rank partials); "[ROCm][MLA][DCP] Support causal multi-token
+ * verification", Implementation item 3 (base-2 statistics -> BF16 output plus
+ * natural-log LSE).
+ *
+ *   part_o, part_m, part_l  dcp_mla_partial's outputs for the same ranks
+ *   out       device bf16 [R][H][512]   out: sum over ranks and splits of
+ *             2^(m-M) l o / sum 2^(m-M) l, rounded to nearest even (0 if empty)
+ *   lse       device float [R][H]       out: natural-log LSE of the merged row,
+ *             -inf if no rank has a token
+ *   rank_lse  device float [nr][R][H]   out (optional, NULL to skip): each
+ *             rank's own natural-log LSE, -inf for an empty rank-local row
+ * With num_ranks < dcp the result merges only the given ranks.
+ */
+dcp_status dcp_lse_merge(const dcp_mla_dims* dims, int32_t num_ranks, const float* part_o,
+                         const float* part_m, const float* part_l, void* out, float* lse,
+                         float* rank_lse, uint32_t* status, dcp_stream_t stream);
+
+/* Message for the last non-OK return on this thread ("" if none). */
+const char* dcp_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCP_MLA_H */
