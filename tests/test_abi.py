@@ -13,9 +13,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def dm():
-    from decode_context_mla_causal_gb300 import build
+    import __graft_entry__
 
-    build.build()
+    __graft_entry__.build()
     import decode_context_mla_causal_gb300 as mod
 
     return mod
