@@ -29,6 +29,7 @@ STATUS_BAD_BLOCK_ID = 0x4
 STATUS_BAD_PAGE = 0x8
 STATUS_TIMEOUT = 0x10
 STATUS_BAD_SPLIT = 0x20
+STATUS_Q_RANGE = 0x40
 
 KV_BF16 = 0
 KV_FP8_E4M3 = 1

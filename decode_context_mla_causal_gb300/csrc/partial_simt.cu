@@ -217,7 +217,7 @@ partial_simt_kernel(int batch, int qlen, int H, int num_splits, int subpage, int
 
 }  // namespace
 
-cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* q,
+cudaError_t launch_partial_simt(const dcp_mla_dims& d, const Derived& x, const void* q,
                            const void* kv, dcp_kv_dtype kv_dtype, const float* kv_scale,
                            float softmax_scale, int num_ranks, const int32_t* row_len,
                            const int32_t* page_ids, const int32_t* split_beg,

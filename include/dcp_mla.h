@@ -88,6 +88,8 @@ typedef enum {
 #define DCP_STATUS_BAD_PAGE 0x8u        /* partial kernel met an invalid page id   */
 #define DCP_STATUS_TIMEOUT 0x10u        /* an on-device wait gave up (bounded)     */
 #define DCP_STATUS_BAD_SPLIT 0x20u      /* split bounds outside [0, MP]            */
+#define DCP_STATUS_Q_RANGE 0x40u        /* |q| > 65504: the FP8-cache path computes
+                                           q.k in f16, which cannot hold it        */
 
 typedef enum { DCP_KV_BF16 = 0, DCP_KV_FP8_E4M3 = 1 } dcp_kv_dtype;
 
@@ -167,7 +169,7 @@ dcp_status dcp_mla_metadata(const dcp_mla_dims* dims, const int32_t* seq_lens,
  *               -inf for an empty split
  *   part_l      device float [nr][NS][R][H]  out: l = sum_t 2^(s_t - m)
  *   status      device uint32 [1]            in/out: DCP_STATUS_BAD_PAGE,
- *               DCP_STATUS_BAD_SPLIT, DCP_STATUS_TIMEOUT
+ *               DCP_STATUS_BAD_SPLIT, DCP_STATUS_TIMEOUT, DCP_STATUS_Q_RANGE
  * Tokens at or beyond a row's length, and pages with invalid ids, never reach
  * the result (invalid ids also set DCP_STATUS_BAD_PAGE).
  */
