@@ -11,33 +11,44 @@
 //   * One 128-row fp32 accumulator over all 512 value dims would fill the SM's
 //     whole tensor memory, leaving no room for the scores. So the value dims are
 //     split: CTA c accumulates O[:, 256c : 256c+256] (256 TMEM columns).
-//   * Both CTAs need the full scores S = Q.K^T. Instead of computing them twice,
-//     the 576 q/k dims are split too: CTA0 computes the partial S over dims
-//     [0, 256), CTA1 over dims [256, 576); each writes its partial into the other
-//     CTA's shared memory (distributed shared memory) and adds the one it gets.
-//     Float addition commutes, so both CTAs hold bit-identical S, run the same
-//     online softmax and agree on P, m and l.
-//   * CTA c stages the dims [256c, 256c + 256 + 64c) of every token: its QK
-//     slice, which also contains its value slice.
+//   * Both CTAs need the full scores. Instead of computing them twice, the 576
+//     q/k dims are split too: CTA0 computes the partial score x0 over dims
+//     [0, 256), CTA1 x1 over dims [256, 576) (log2 units). Shared memory across
+//     the pair is slow (about 25 GB/s per SM each way), so a CTA does not send x
+//     itself: for each (row, 32-token half) it sends its own maximum m_c and the
+//     factors E_c = 2^(x_c - m_c) in f16 (scaled by 2^14, so values down to
+//     2^-28 keep 11 bits). The receiver forms
+//         p = E_own * E_peer * 2^(m_own + m_peer - M),
+//     where M is the running reference, updated only when the tile bound
+//     m_own + m_peer exceeds it by more than 8 (then O and l are rescaled). The
+//     bound is an upper bound of the true maximum, so p <= 2^8. Relative error
+//     of p and l from the f16 factor: at most 2^-12. Both CTAs agree on M (sums of
+//     the same two floats), so their l and P agree to that error; each CTA
+//     normalises its own half of O by its own l.
+//   * CTA c stages dims [256c, 256c + 256 + 64c) of every token: its q.k slice,
+//     which also holds its value slice.
 //
-// Per CTA (288 threads):
-//   warps 0-3  softmax: thread r owns tile row r (TMEM lane r); loads Q into
-//              TMEM, exchanges partial scores, online base-2 softmax with lazy
-//              rescaling, writes P (16-bit) into TMEM, final epilogue.
-//   warps 4-7  KV producers: 16-byte loads of the paged cache rows (subpage ids
-//              from the metadata, bounds-checked), FP8 E4M3 -> f16 conversion,
-//              stores into 128-byte-swizzled K-major tiles of a 4-stage ring.
-//   warp 8     TMEM allocation and the single MMA-issuing thread:
-//              S  = Q[tmem] . K_tile^T        (M=128, N=64,  K=16 per MMA)
-//              O += P[tmem] . V_tile          (M=128, N=256, V read MN-major
-//                                              from the same swizzled tile)
+// Per CTA (416 threads):
+//   warps 0-7   softmax: warp w owns rows 32*(w%4) .. +31 (TMEM lane quarter)
+//               and token half w/4 of every 64-token tile; Q into TMEM, factor
+//               exchange (double-buffered slots), lazy online softmax, P
+//               (16-bit) into TMEM, epilogue for O columns [128*(w/4), +128).
+//   warps 8-11  KV producers: 16-byte loads of the paged cache rows (subpage ids
+//               from the metadata, bounds-checked, two tiles in flight), FP8
+//               E4M3 -> f16 conversion, stores into 128-byte-swizzled K-major
+//               tiles of a 4-stage ring.
+//   warp 12     TMEM allocation and the single MMA-issuing thread:
+//               S  = Q[tmem] . K_tile^T        (M=128, N=64,  K=16 per MMA)
+//               O += P[tmem] . V_tile          (M=128, N=256, V read MN-major
+//                                               from the same swizzled tile)
 // TMEM columns: O [0,256), S [256,320), P [320,352), Q [352, 352 + 32*atoms).
 // The FP8-cache path computes in f16 (E4M3 -> f16 is exact; q is BF16 -> f16,
 // exact in f16's normal range; |q| > 65504 sets DCP_STATUS_Q_RANGE); the BF16
 // cache path computes in bf16. Accumulation is fp32 throughout.
 //
 // Every wait is bounded (DCP_STATUS_TIMEOUT and an orderly exit: all roles stop,
-// in-flight MMAs are drained, TMEM is freed). Nothing traps.
+// in-flight MMAs are drained, TMEM is freed). Waiting threads sleep in
+// mbarrier.try_wait instead of spinning. Nothing traps.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -56,11 +67,19 @@ constexpr int kStages = 4;     // KV ring depth
 constexpr int kMaxAtoms = 5;   // 64-dim swizzle atoms staged per CTA (CTA1: 320 dims)
 constexpr int kAtomBytes = kTileN * 128;
 constexpr int kStageBytes = kMaxAtoms * kAtomBytes;
-constexpr int kXchBytes = kTileN * kRows * 4;
-constexpr int kThreads = 288;
+// factor exchange slot: E as f16 [half 2][group 4][row 128][8 values], m as f32 [half][row]
+constexpr int kXchEBytes = 2 * 4 * kRows * 16;
+constexpr int kXchSlotBytes = kXchEBytes + 2 * kRows * 4;
+constexpr int kXchSlots = 2;
+constexpr int kCombBytes = 2 * 2 * kRows * 4;  // [parity][half][row] f32 for the half combine
+constexpr int kSoftWarps = 8;
+constexpr int kProdWarp0 = 8;
+constexpr int kMmaWarp = 12;
+constexpr int kThreads = 13 * 32;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // P may grow to 2^8 before O is rescaled
+constexpr float kFactorScale = 16384.0f;   // 2^14: keeps E down to 2^-28 normal in f16
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -73,14 +92,15 @@ enum {
   kBarPFull,
   kBarODone,
   kBarQFull,
-  kBarXFull,   // the peer's partial scores are in my exchange buffer
-  kBarXFree,   // the peer has consumed what I wrote into its buffer
-  kBarDrain,
+  kBarXFull,                     // [2] the peer's factors are in my slot
+  kBarXFree = kBarXFull + kXchSlots,  // [2] the peer consumed what I wrote into its slot
+  kBarComb = kBarXFree + kXchSlots,  // [4 lane quarters][2 parities] half-combine, count 64
+  kBarDrain = kBarComb + 8,
   kNumBars
 };
 
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kXchBytes +
-                              kNumBars * 8 + 16;
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes +
+                              kXchSlots * kXchSlotBytes + kCombBytes + kNumBars * 8 + 16;
 
 struct Params {
   const uint16_t* q;
@@ -101,7 +121,8 @@ struct Params {
 
 struct Shared {
   uint8_t* stages;
-  float* xbuf;
+  uint8_t* xch;  // kXchSlots slots
+  float* comb;
   uint64_t* bars;
   uint32_t* tmem_slot;
   int* abort_flag;
@@ -112,32 +133,37 @@ __device__ __forceinline__ Shared carve(unsigned char* raw) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   s.stages = base;
-  s.xbuf = reinterpret_cast<float*>(base + kStages * kStageBytes);
-  s.bars = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes + kXchBytes);
+  s.xch = base + kStages * kStageBytes;
+  s.comb = reinterpret_cast<float*>(s.xch + kXchSlots * kXchSlotBytes);
+  s.bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.comb) + kCombBytes);
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + kNumBars);
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
   return s;
 }
 
-// Bounded wait on an mbarrier phase. Returns false (after raising the abort flag
-// and DCP_STATUS_TIMEOUT) if the phase does not complete within kTimeoutNs, or
-// at once if another thread of the CTA has already aborted.
-__device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, int* abort_flag,
-                                        uint32_t* status, bool cluster_acquire) {
-  const uint32_t a = smem_u32(bar);
-  if (cluster_acquire ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
+// Bounded wait on an mbarrier phase. The slow path sleeps in try_wait (with a
+// suspend-time hint) instead of spinning, gives up after kTimeoutNs (raising the
+// abort flag and DCP_STATUS_TIMEOUT), and returns false at once when another
+// thread of the CTA has already aborted.
+__device__ __noinline__ bool wait_phase_slow(uint32_t a, uint32_t parity, int* abort_flag,
+                                             uint32_t* status, bool cluster_acquire) {
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (cluster_acquire ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
-      if (globaltimer_ns() - t0 > kTimeoutNs) {
-        *reinterpret_cast<volatile int*>(abort_flag) = 1;
-        raise_status(status, DCP_STATUS_TIMEOUT);
-        return false;
-      }
+  for (;;) {
+    if (cluster_acquire ? mbar_wait_sleep_cluster(a, parity) : mbar_wait_sleep(a, parity))
+      return true;
+    if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
+    if (globaltimer_ns() - t0 > kTimeoutNs) {
+      *reinterpret_cast<volatile int*>(abort_flag) = 1;
+      raise_status(status, DCP_STATUS_TIMEOUT);
+      return false;
     }
   }
+}
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, int* abort_flag,
+                                           uint32_t* status, bool cluster_acquire) {
+  const uint32_t a = smem_u32(bar);
+  if (cluster_acquire ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
+  return wait_phase_slow(a, parity, abort_flag, status, cluster_acquire);
 }
 
 struct Item {
@@ -173,6 +199,14 @@ __device__ __forceinline__ Item decode_item(const Params& p, int cluster_id) {
   return it;
 }
 
+// 2^x on the MUFU unit (ex2.approx, flush-to-zero); x <= 8 here and results
+// below 2^-126 only ever meet other tiny weights.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // E4M3 x2 -> f16 x2 (exact): the hardware conversion.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_bytes & 0xFFFFu), __NV_E4M3);
@@ -180,87 +214,136 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
 }
 
 // ----------------------------------------------------------------- producers
-template <bool kFp8>
-__device__ __forceinline__ void run_producer(const Params& p, const Shared& sh, const Item& it,
-                                             int cta, int ct) {
-  constexpr int kElem = kFp8 ? 1 : 2;
-  const int n_atoms = 4 + cta;
-  const int d0 = 256 * cta;
-  // 16-byte pieces per token: FP8 -> 4 per atom (16 dims), BF16 -> 8 per atom (8 dims)
-  const int ppt = n_atoms * (kFp8 ? 4 : 8);
-  const int pieces = kTileN * ppt;
-  constexpr int kMaxLoads = kFp8 ? (kTileN * kMaxAtoms * 4) / 128 : (kTileN * kMaxAtoms * 8) / 128;
-  const int R = p.batch * p.qlen;
-  (void)R;
-  const int64_t pool_pages = p.pool_rows / p.subpage;
-  const uint8_t* pool = p.kv + (int64_t)it.k * p.pool_rows * kDqk * kElem;
-  const int32_t* pages = p.page_ids + ((int64_t)it.k * p.batch + it.b) * p.max_pages;
-  bool bad_page = false;
-  for (int i = 0; i < it.n_tiles; ++i) {
-    const int st = i % kStages;
+// One work unit is one 16-byte global load. FP8: unit u -> quarter u&3 (16 dims,
+// two 16-byte f16 chunks), token (u>>2)&63, atom u>>8. BF16: unit u -> chunk u&7
+// (8 dims), token (u>>3)&63, atom u>>9. A warp thus covers 8 (FP8) or 4 (BF16)
+// consecutive tokens of one atom: 64-byte (or 128-byte) contiguous global reads
+// per token, and shared stores that fill whole 128-byte swizzled rows (no bank
+// conflicts beyond the four wavefronts a 512-byte warp store needs).
+template <bool kFp8, int kAtoms>
+struct Producer {
+  static constexpr int kElem = kFp8 ? 1 : 2;
+  static constexpr int kD0 = 256 * (kAtoms - 4);  // first staged dim: 0 (CTA0) or 256 (CTA1)
+  static constexpr int kUnitsPerAtom = kFp8 ? 256 : 512;
+  static constexpr int kLoads = kAtoms * kUnitsPerAtom / 128;
+
+  const Params& p;
+  const Shared& sh;
+  const Item& it;
+  int ct, lg_sub;
+  int64_t pool_pages;
+  const uint8_t* pool;
+  const int32_t* pages;
+  bool big_pages, bad_page;
+
+  __device__ __forceinline__ Producer(const Params& p_, const Shared& sh_, const Item& it_, int ct_)
+      : p(p_), sh(sh_), it(it_), ct(ct_) {
+    lg_sub = __ffs(p.subpage) - 1;
+    pool_pages = p.pool_rows >> lg_sub;
+    pool = p.kv + (int64_t)it.k * p.pool_rows * kDqk * kElem;
+    pages = p.page_ids + ((int64_t)it.k * p.batch + it.b) * p.max_pages;
+    big_pages = p.subpage >= kTileN;  // then a tile lies inside one subpage
+    bad_page = false;
+  }
+
+  __device__ __forceinline__ int32_t tile_page(int i) const {
+    if (!big_pages || i >= it.n_tiles) return -1;
+    return __ldg(pages + ((it.t_start + i * kTileN) >> lg_sub));
+  }
+
+  __device__ __forceinline__ void load(int i, int32_t pg_tile, uint4 (&v)[kLoads]) {
     const int tok0 = it.t_start + i * kTileN;
-    uint4 v[kMaxLoads];
 #pragma unroll
-    for (int l = 0; l < kMaxLoads; ++l) {
-      const int f = l * 128 + ct;
+    for (int l = 0; l < kLoads; ++l) {
+      const int u = l * 128 + ct;
+      int tk, off;
+      if (kFp8) {
+        tk = (u >> 2) & 63;
+        off = kD0 + (u >> 8) * 64 + (u & 3) * 16;
+      } else {
+        tk = (u >> 3) & 63;
+        off = (kD0 + (u >> 9) * 64 + (u & 7) * 8) * 2;
+      }
+      const int li = tok0 + tk;
       v[l] = make_uint4(0u, 0u, 0u, 0u);
-      if (f < pieces) {
-        const int tk = f / ppt, pc = f % ppt;
-        const int li = tok0 + tk;
-        if (li < it.t_end) {
-          const int32_t pg = pages[li / p.subpage];
-          if (pg >= 0 && pg < pool_pages) {
-            const uint8_t* src = pool + (((int64_t)pg * p.subpage + li % p.subpage) * kDqk + d0) * kElem +
-                                 pc * 16;
-            v[l] = __ldg(reinterpret_cast<const uint4*>(src));
-          } else {
-            bad_page = true;
-          }
+      if (li < it.t_end) {
+        const int32_t pg = big_pages ? pg_tile : __ldg(pages + (li >> lg_sub));
+        if (pg >= 0 && pg < pool_pages) {
+          const int64_t row = ((int64_t)pg << lg_sub) + (li & (p.subpage - 1));
+          v[l] = __ldg(reinterpret_cast<const uint4*>(pool + row * (kDqk * kElem) + off));
+        } else {
+          bad_page = true;
         }
       }
     }
-    if (i >= kStages) {
-      if (!wait_phase(&sh.bars[kBarKvEmpty + st], ((i / kStages) - 1) & 1, sh.abort_flag, p.status,
-                      false))
-        break;
-    }
+  }
+
+  __device__ __forceinline__ bool store(int i, const uint4 (&v)[kLoads]) {
+    const int st = i % kStages;
+    if (i >= kStages && !wait_phase(&sh.bars[kBarKvEmpty + st], ((i / kStages) - 1) & 1,
+                                    sh.abort_flag, p.status, false))
+      return false;
     uint8_t* stage = sh.stages + st * kStageBytes;
 #pragma unroll
-    for (int l = 0; l < kMaxLoads; ++l) {
-      const int f = l * 128 + ct;
-      if (f < pieces) {
-        const int tk = f / ppt, pc = f % ppt;
-        if (kFp8) {
-          const int atom = pc >> 2, ch = (pc & 3) * 2;
-          uint4 lo, hi;
-          lo.x = e4m3x2_to_f16x2(v[l].x);
-          lo.y = e4m3x2_to_f16x2(v[l].x >> 16);
-          lo.z = e4m3x2_to_f16x2(v[l].y);
-          lo.w = e4m3x2_to_f16x2(v[l].y >> 16);
-          hi.x = e4m3x2_to_f16x2(v[l].z);
-          hi.y = e4m3x2_to_f16x2(v[l].z >> 16);
-          hi.z = e4m3x2_to_f16x2(v[l].w);
-          hi.w = e4m3x2_to_f16x2(v[l].w >> 16);
-          uint8_t* a = stage + atom * kAtomBytes;
-          *reinterpret_cast<uint4*>(a + sw128_offset(tk, ch)) = lo;
-          *reinterpret_cast<uint4*>(a + sw128_offset(tk, ch + 1)) = hi;
-        } else {
-          const int atom = pc >> 3, ch = pc & 7;
-          *reinterpret_cast<uint4*>(stage + atom * kAtomBytes + sw128_offset(tk, ch)) = v[l];
-        }
+    for (int l = 0; l < kLoads; ++l) {
+      const int u = l * 128 + ct;
+      if (kFp8) {
+        const int qq = u & 3, tk = (u >> 2) & 63, a = u >> 8;
+        uint4 lo, hi;
+        lo.x = e4m3x2_to_f16x2(v[l].x);
+        lo.y = e4m3x2_to_f16x2(v[l].x >> 16);
+        lo.z = e4m3x2_to_f16x2(v[l].y);
+        lo.w = e4m3x2_to_f16x2(v[l].y >> 16);
+        hi.x = e4m3x2_to_f16x2(v[l].z);
+        hi.y = e4m3x2_to_f16x2(v[l].z >> 16);
+        hi.z = e4m3x2_to_f16x2(v[l].w);
+        hi.w = e4m3x2_to_f16x2(v[l].w >> 16);
+        uint8_t* at = stage + a * kAtomBytes;
+        *reinterpret_cast<uint4*>(at + sw128_offset(tk, 2 * qq)) = lo;
+        *reinterpret_cast<uint4*>(at + sw128_offset(tk, 2 * qq + 1)) = hi;
+      } else {
+        const int ch = u & 7, tk = (u >> 3) & 63, a = u >> 9;
+        *reinterpret_cast<uint4*>(stage + a * kAtomBytes + sw128_offset(tk, ch)) = v[l];
       }
     }
     fence_proxy_async_smem();
     mbar_arrive(&sh.bars[kBarKvFull + st]);
+    return true;
   }
-  if (bad_page) raise_status(p.status, DCP_STATUS_BAD_PAGE);
-}
+
+  // FP8: two register buffers, so tile i+1's loads are in flight while tile i is
+  // converted and stored; tile pages are read two tiles ahead. BF16 (twice the
+  // registers per tile): one buffer.
+  __device__ __forceinline__ void run() {
+    const int n = it.n_tiles;
+    if (kFp8) {
+      uint4 va[kLoads], vb[kLoads];
+      int32_t pg1 = tile_page(1);
+      load(0, tile_page(0), va);
+      for (int i = 0; i < n; i += 2) {
+        const int32_t pg2 = tile_page(i + 2);
+        if (i + 1 < n) load(i + 1, pg1, vb);
+        if (!store(i, va) || i + 1 >= n) break;
+        pg1 = tile_page(i + 3);
+        if (i + 2 < n) load(i + 2, pg2, va);
+        if (!store(i + 1, vb)) break;
+      }
+    } else {
+      uint4 v[kLoads];
+      for (int i = 0; i < n; ++i) {
+        load(i, tile_page(i), v);
+        if (!store(i, v)) break;
+      }
+    }
+    if (bad_page) raise_status(p.status, DCP_STATUS_BAD_PAGE);
+  }
+};
 
 // ----------------------------------------------------------------- MMA issuer
-template <bool kFp8>
-__device__ __forceinline__ void run_mma(const Params& p, const Shared& sh, const Item& it, int cta,
+template <bool kFp8, int kAtoms>
+__device__ __forceinline__ void run_mma(const Params& p, const Shared& sh, const Item& it,
                                         uint32_t tbase) {
-  const int n_atoms = 4 + cta;
+  constexpr int n_atoms = kAtoms;
   const uint32_t idq = idesc_f16(kRows, kTileN, !kFp8, false);
   const uint32_t idp = idesc_f16(kRows, 256, !kFp8, true);
   const uint32_t stage0 = smem_u32(sh.stages);
@@ -287,6 +370,7 @@ __device__ __forceinline__ void run_mma(const Params& p, const Shared& sh, const
       break;
     tc_fence_after();
     const uint32_t sa = stage0 + st * kStageBytes;
+#pragma unroll
     for (int kk = 0; kk < n_atoms * 4; ++kk) {
       const uint64_t d = smem_desc_sw128(sa + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024);
       mma_f16_ts(tbase + kColS, tbase + kColQ + 8 * kk, d, idq, kk > 0 ? 1u : 0u);
@@ -308,45 +392,53 @@ __device__ __forceinline__ void run_mma(const Params& p, const Shared& sh, const
 }
 
 // ----------------------------------------------------------------- softmax
-template <bool kFp8>
+template <bool kFp8, int kAtoms>
 __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, const Item& it,
-                                            int cta, uint32_t tbase, int r) {
-  const int warp = r >> 5;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  const uint32_t tS = tbase + lane_off + kColS;
-  const uint32_t tP = tbase + lane_off + kColP;
-  const uint32_t tO = tbase + lane_off + kColO;
+                                            uint32_t tbase, int tid) {
+  constexpr int cta = kAtoms - 4;
+  constexpr int d0 = 256 * cta;
+  constexpr int kAtomsLo = (kAtoms + 1) / 2;  // Q atoms loaded by half 0
+  const int warp = tid >> 5, lane = tid & 31;
+  const int qw = warp & 3;   // TMEM lane quarter
+  const int h = warp >> 2;   // token half of each tile / O column half
+  const int r = qw * 32 + lane;
+  const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+  const uint32_t tS = tbase + lane_off + kColS + 32 * h;
+  const uint32_t tP = tbase + lane_off + kColP + 16 * h;
+  const uint32_t tO = tbase + lane_off + kColO + 128 * h;
   const uint32_t tQ = tbase + lane_off + kColQ;
-  const int n_atoms = 4 + cta;
-  const int d0 = 256 * cta;
   const int qrows = p.qlen * p.H;
   const int R = p.batch * p.qlen;
   const bool row_ok = r < it.rows_valid;
   const int qr = it.qr0 + r;
   const int j = row_ok ? qr / p.H : 0;
   const int L = row_ok ? p.row_len[(int64_t)it.k * R + (int64_t)it.b * p.qlen + j] : 0;
+  const int row_end = min(L, it.t_end);  // tokens at or past it are invisible to this row
   const float kv_scale = p.kv_scale ? *p.kv_scale : 1.0f;
   const float sc = p.softmax_scale * kv_scale * kLog2e;
 
-  // Q slice -> TMEM (16-bit pairs along the dims, lane = row)
+  // Q slice -> TMEM (16-bit pairs along the dims, lane = row); half h loads its atoms
   {
     const uint16_t* src = p.q + ((int64_t)it.b * qrows + qr) * kDqk + d0;
     bool q_range = false;
-    for (int a = 0; a < n_atoms; ++a) {
+    const int a0 = h == 0 ? 0 : kAtomsLo;
+    const int a1 = h == 0 ? kAtomsLo : kAtoms;
+#pragma unroll 1
+    for (int a = a0; a < a1; ++a) {
       uint32_t w[32];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (row_ok) v = __ldg(reinterpret_cast<const uint4*>(src + a * 64 + c * 8));
-        uint32_t x[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           if (kFp8) {
             const float f0 = __uint_as_float(x[e] << 16);
             const float f1 = __uint_as_float(x[e] & 0xFFFF0000u);
             q_range |= fabsf(f0) > 65504.f || fabsf(f1) > 65504.f;
-            __half2 h = __floats2half2_rn(f0, f1);
-            w[c * 4 + e] = *reinterpret_cast<uint32_t*>(&h);
+            __half2 hh = __floats2half2_rn(f0, f1);
+            w[c * 4 + e] = *reinterpret_cast<uint32_t*>(&hh);
           } else {
             w[c * 4 + e] = x[e];
           }
@@ -360,120 +452,152 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
     mbar_arrive(&sh.bars[kBarQFull]);
   }
 
-  const int peer = cta ^ 1;
-  const uint32_t x_local = smem_u32(sh.xbuf);
-  const uint32_t x_remote = mapa_shared(x_local, peer);
+  const uint32_t peer = cta ^ 1;
+  const uint32_t xch_local = smem_u32(sh.xch);
+  const uint32_t xch_remote = mapa_shared(xch_local, peer);
   const uint32_t xfull_remote = mapa_shared(smem_u32(&sh.bars[kBarXFull]), peer);
   const uint32_t xfree_remote = mapa_shared(smem_u32(&sh.bars[kBarXFree]), peer);
   const int32_t* pages = p.page_ids + ((int64_t)it.k * p.batch + it.b) * p.max_pages;
-  const int64_t pool_pages = p.pool_rows / p.subpage;
+  const int lg_sub = __ffs(p.subpage) - 1;
+  const int64_t pool_pages = p.pool_rows >> lg_sub;
+  const bool big_pages = p.subpage >= kTileN;
+  // The two warps sharing rows (w and w^4) combine per-row values through smem,
+  // synchronised by an mbarrier per (lane quarter, parity) with bounded waits.
+  auto pair_sync = [&](int i) -> bool {
+    uint64_t* bar = &sh.bars[kBarComb + qw * 2 + (i & 1)];
+    mbar_arrive(bar);
+    return __all_sync(0xffffffffu, wait_phase(bar, (i >> 1) & 1, sh.abort_flag, p.status, false));
+  };
 
   // Waits are made warp-uniform: the tcgen05.ld/st that follow are warp-collective.
   auto wait_warp = [&](int bar, uint32_t parity, bool cluster) -> bool {
-    return __all_sync(0xffffffffu, wait_phase(&sh.bars[bar], parity, sh.abort_flag, p.status, cluster));
+    return __all_sync(0xffffffffu,
+                      wait_phase(&sh.bars[bar], parity, sh.abort_flag, p.status, cluster));
   };
-  float m_run = -INFINITY, l_run = 0.f;
+  float M = -INFINITY;  // running reference (log2 units), same in both CTAs
+  float l_half = 0.f;   // sum of this half's weights
   bool ok = true;
+  int32_t pg_next = (big_pages && it.n_tiles > 0) ? __ldg(pages + (it.t_start >> lg_sub)) : 0;
   for (int i = 0; i < it.n_tiles; ++i) {
+    const int tok0 = it.t_start + i * kTileN;
+    const int32_t pg_tile = pg_next;
     if (!wait_warp(kBarSFull, i & 1, false)) {
       ok = false;
       break;
     }
     tc_fence_after();
-    uint32_t s0[32], s1[32];
-    tmem_ld32(tS, s0);
-    tmem_ld32(tS + 32, s1);
-    tmem_wait_ld(s0);
-    tmem_wait_ld(s1);
+    uint32_t s[32];
+    tmem_ld32(tS, s);
+    tmem_wait_ld(s);
     tc_fence_before();
     mbar_arrive(&sh.bars[kBarSFree]);
 
-    // exchange partial scores with the peer CTA
-    if (i >= 1 && !wait_warp(kBarXFree, (i - 1) & 1, true)) {
-      ok = false;
-      break;
-    }
-#pragma unroll
-    for (int g = 0; g < 8; ++g)
-      st_cluster_v4(x_remote + (uint32_t)((g * kRows + r) * 16), s0[4 * g], s0[4 * g + 1],
-                    s0[4 * g + 2], s0[4 * g + 3]);
-#pragma unroll
-    for (int g = 0; g < 8; ++g)
-      st_cluster_v4(x_remote + (uint32_t)(((8 + g) * kRows + r) * 16), s1[4 * g], s1[4 * g + 1],
-                    s1[4 * g + 2], s1[4 * g + 3]);
-    mbar_arrive_remote(xfull_remote);
-    if (!wait_warp(kBarXFull, i & 1, true)) {
-      ok = false;
-      break;
-    }
-    float sv[64];
-#pragma unroll
-    for (int g = 0; g < 16; ++g) {
-      const float4 o = *reinterpret_cast<const float4*>(sh.xbuf + (g * kRows + r) * 4);
-      const uint32_t* mine = g < 8 ? &s0[4 * g] : &s1[4 * (g - 8)];
-      sv[4 * g + 0] = __uint_as_float(mine[0]) + o.x;
-      sv[4 * g + 1] = __uint_as_float(mine[1]) + o.y;
-      sv[4 * g + 2] = __uint_as_float(mine[2]) + o.z;
-      sv[4 * g + 3] = __uint_as_float(mine[3]) + o.w;
-    }
-    mbar_arrive_remote(xfree_remote);
-
-    // which of the 64 tokens are visible to this row
-    const int tok0 = it.t_start + i * kTileN;
-    uint64_t vis;
-    {
-      const int cnt_split = min(kTileN, it.t_end - tok0);
-      const int cnt_row = max(0, min(cnt_split, L - tok0));
-      vis = cnt_row >= 64 ? ~0ull : ((1ull << cnt_row) - 1ull);
-      if (p.subpage >= kTileN) {
-        const int32_t pg = pages[tok0 / p.subpage];
-        if (pg < 0 || pg >= pool_pages) vis = 0;
-      } else {
-        const int np = (cnt_split + p.subpage - 1) / p.subpage;
-        for (int q = 0; q < np; ++q) {
-          const int32_t pg = pages[tok0 / p.subpage + q];
-          if (pg < 0 || pg >= pool_pages) {
-            const uint64_t m = (p.subpage >= 64 ? ~0ull : ((1ull << p.subpage) - 1ull))
-                               << (q * p.subpage);
-            vis &= ~m;
-          }
+    // visible tokens of this row in this half: [tok0 + 32h, row_end), pages valid
+    const int cnt = max(0, min(32, row_end - tok0 - 32 * h));
+    uint32_t vis = cnt >= 32 ? 0xFFFFFFFFu : ((1u << cnt) - 1u);
+    if (big_pages) {
+      if (pg_tile < 0 || pg_tile >= pool_pages) vis = 0;
+    } else if (vis) {
+      const int first = (tok0 + 32 * h) >> lg_sub;
+      const int last = (tok0 + 32 * h + cnt - 1) >> lg_sub;
+      for (int q = first; q <= last; ++q) {
+        const int32_t pg = pages[q];
+        if (pg < 0 || pg >= pool_pages) {
+          const int lo = max(0, (q << lg_sub) - (tok0 + 32 * h));
+          const int hi = min(32, ((q + 1) << lg_sub) - (tok0 + 32 * h));
+          const uint32_t m = (hi - lo >= 32) ? 0xFFFFFFFFu : (((1u << (hi - lo)) - 1u) << lo);
+          vis &= ~m;
         }
       }
     }
-    float m_tile = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      sv[c] *= sc;
-      if ((vis >> c) & 1ull) m_tile = fmaxf(m_tile, sv[c]);
-    }
-    const float m_new = fmaxf(m_run, m_tile);
-    const bool need = m_new > m_run + kRescaleThreshold || (m_run == -INFINITY && m_new != -INFINITY);
-    float alpha = 1.f;
-    if (need) {
-      alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
-      l_run *= alpha;
-      m_run = m_new;
-    }
-    uint32_t pk[32];
-    float lsum = 0.f;
+    float x[32];
+    float m_own = -INFINITY;
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
-      const bool v0 = (vis >> (2 * c)) & 1ull, v1 = (vis >> (2 * c + 1)) & 1ull;
-      const float p0 = v0 ? exp2f(sv[2 * c] - m_run) : 0.f;
-      const float p1 = v1 ? exp2f(sv[2 * c + 1] - m_run) : 0.f;
+      x[c] = __uint_as_float(s[c]) * sc;
+      if ((vis >> c) & 1u) m_own = fmaxf(m_own, x[c]);
+    }
+    // own factors E = 2^(x - m_own) (fp32, kept), sent as f16 * 2^14
+    uint32_t e16[16];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) x[c] = ((vis >> c) & 1u) ? fast_exp2(x[c] - m_own) : 0.f;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      __half2 hh = __floats2half2_rn(x[2 * c] * kFactorScale, x[2 * c + 1] * kFactorScale);
+      e16[c] = *reinterpret_cast<uint32_t*>(&hh);
+    }
+    // send to the peer's slot (i & 1); it must have consumed what it held two tiles ago
+    const int slot = i & 1;
+    if (i >= 2 && !wait_warp(kBarXFree + slot, ((i >> 1) - 1) & 1, true)) {
+      ok = false;
+      break;
+    }
+    {
+      const uint32_t dst = xch_remote + slot * kXchSlotBytes;
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+        st_cluster_v4(dst + (uint32_t)(((h * 4 + g) * kRows + r) * 16), e16[4 * g],
+                      e16[4 * g + 1], e16[4 * g + 2], e16[4 * g + 3]);
+      const uint32_t mdst = dst + kXchEBytes + (uint32_t)((h * kRows + r) * 4);
+      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(mdst), "f"(m_own) : "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(xfull_remote + 8 * slot);  // releases the warp's stores
+    }
+    if (!wait_warp(kBarXFull + slot, (i >> 1) & 1, true)) {
+      ok = false;
+      break;
+    }
+    uint4 pe[4];
+    float m_peer;
+    {
+      const uint8_t* src = sh.xch + slot * kXchSlotBytes;
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+        pe[g] = *reinterpret_cast<const uint4*>(src + ((h * 4 + g) * kRows + r) * 16);
+      m_peer = *reinterpret_cast<const float*>(src + kXchEBytes + (h * kRows + r) * 4);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(xfree_remote + 8 * slot);
+    }
+    // tile bound of the row (max over both halves of m_own + m_peer)
+    const float ub_h = (m_own == -INFINITY || m_peer == -INFINITY) ? -INFINITY : m_own + m_peer;
+    float* comb = sh.comb + (i & 1) * 2 * kRows;
+    comb[h * kRows + r] = ub_h;
+    if (!pair_sync(i)) {
+      ok = false;
+      break;
+    }
+    const float ub = fmaxf(ub_h, comb[(h ^ 1) * kRows + r]);
+    const bool need = ub != -INFINITY && (M == -INFINITY || ub > M + kRescaleThreshold);
+    float alpha = 1.f;
+    if (need) {
+      alpha = M == -INFINITY ? 0.f : fast_exp2(M - ub);
+      l_half *= alpha;
+      M = ub;
+    }
+    // p = E_own * E_peer * 2^(m_own + m_peer - M)  (E_peer carries 2^14)
+    const float f = ub_h == -INFINITY ? 0.f : fast_exp2(ub_h - M) * (1.0f / kFactorScale);
+    uint32_t pk[16];
+    float lsum = 0.f;
+    const uint32_t pw[16] = {pe[0].x, pe[0].y, pe[0].z, pe[0].w, pe[1].x, pe[1].y,
+                             pe[1].z, pe[1].w, pe[2].x, pe[2].y, pe[2].z, pe[2].w,
+                             pe[3].x, pe[3].y, pe[3].z, pe[3].w};
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const float2 ep = __half22float2(*reinterpret_cast<const __half2*>(&pw[c]));
+      const float p0 = x[2 * c] * ep.x * f;
+      const float p1 = x[2 * c + 1] * ep.y * f;
+      // l sums the fp32 weights; the P.V contraction uses P rounded to 16 bits
+      lsum += p0 + p1;
       if (kFp8) {
-        __half2 h = __floats2half2_rn(p0, p1);
-        const float2 back = __half22float2(h);
-        lsum += back.x + back.y;
-        pk[c] = *reinterpret_cast<uint32_t*>(&h);
+        __half2 hh = __floats2half2_rn(p0, p1);
+        pk[c] = *reinterpret_cast<uint32_t*>(&hh);
       } else {
-        __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-        const float2 back = __bfloat1622float2(h);
-        lsum += back.x + back.y;
-        pk[c] = *reinterpret_cast<uint32_t*>(&h);
+        __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+        pk[c] = *reinterpret_cast<uint32_t*>(&hh);
       }
     }
-    l_run += lsum;
+    l_half += lsum;
+    if (big_pages && i + 1 < it.n_tiles) pg_next = __ldg(pages + ((tok0 + kTileN) >> lg_sub));
     // PV(i-1) done: P buffer is free and O is stable
     if (i >= 1 && !wait_warp(kBarODone, (i - 1) & 1, false)) {
       ok = false;
@@ -482,33 +606,37 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
     tc_fence_after();
     if (i >= 1 && __any_sync(0xffffffffu, need)) {
       const float a = need ? alpha : 1.f;
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t o[32];
-        tmem_ld32(tO + 32 * c8, o);
+        tmem_ld32(tO + 32 * c4, o);
         tmem_wait_ld(o);
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
-        tmem_st32(tO + 32 * c8, o);
+        tmem_st32(tO + 32 * c4, o);
       }
     }
-    tmem_st32(tP, pk);
+    tmem_st16(tP, pk);
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(&sh.bars[kBarPFull]);
   }
 
-  // epilogue: normalised partial output of this CTA's 256 value dims
+  // epilogue: both halves' l, then this warp's 128 O columns of its rows
   const bool have_o = __all_sync(0xffffffffu, ok) && it.n_tiles > 0 &&
                       wait_warp(kBarODone, (it.n_tiles - 1) & 1, false);
   tc_fence_after();
+  float* comb = sh.comb + (it.n_tiles & 1) * 2 * kRows;
+  comb[h * kRows + r] = l_half;
+  const bool paired = pair_sync(it.n_tiles);
+  const float l_run = l_half + comb[(h ^ 1) * kRows + r];
   const int64_t rh = (int64_t)it.b * qrows + qr;
   const int64_t base = ((int64_t)it.k * p.num_splits + it.s) * ((int64_t)R * p.H) + rh;
-  const float inv = l_run > 0.f ? kv_scale / l_run : 0.f;
-  float* dst = p.part_o + base * kDv + 256 * cta;
-  for (int c8 = 0; c8 < 8; ++c8) {
+  const float inv = (paired && l_run > 0.f) ? kv_scale / l_run : 0.f;
+  float* dst = p.part_o + base * kDv + 256 * cta + 128 * h;
+  for (int c4 = 0; c4 < 4; ++c4) {
     uint32_t o[32];
     if (have_o) {
-      tmem_ld32(tO + 32 * c8, o);
+      tmem_ld32(tO + 32 * c4, o);
       tmem_wait_ld(o);
     } else {
 #pragma unroll
@@ -517,14 +645,14 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
     if (row_ok) {
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
-        float4 f = make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+        float4 v = make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
                                __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-        *reinterpret_cast<float4*>(dst + 32 * c8 + e) = f;
+        *reinterpret_cast<float4*>(dst + 32 * c4 + e) = v;
       }
     }
   }
-  if (row_ok && cta == 0) {
-    p.part_m[base] = l_run > 0.f ? m_run : -INFINITY;
+  if (row_ok && cta == 0 && h == 0) {
+    p.part_m[base] = l_run > 0.f ? M : -INFINITY;
     p.part_l[base] = l_run;
   }
 }
@@ -545,12 +673,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&sh.bars[kBarKvEmpty + i], 1);
     }
     mbar_init(&sh.bars[kBarSFull], 1);
-    mbar_init(&sh.bars[kBarSFree], 128);
-    mbar_init(&sh.bars[kBarPFull], 128);
+    mbar_init(&sh.bars[kBarSFree], kSoftWarps * 32);
+    mbar_init(&sh.bars[kBarPFull], kSoftWarps * 32);
     mbar_init(&sh.bars[kBarODone], 1);
-    mbar_init(&sh.bars[kBarQFull], 128);
-    mbar_init(&sh.bars[kBarXFull], 128);
-    mbar_init(&sh.bars[kBarXFree], 128);
+    mbar_init(&sh.bars[kBarQFull], kSoftWarps * 32);
+    for (int i = 0; i < kXchSlots; ++i) {
+      mbar_init(&sh.bars[kBarXFull + i], kSoftWarps);  // one elected arrival per peer warp
+      mbar_init(&sh.bars[kBarXFree + i], kSoftWarps);
+    }
+    for (int i = 0; i < 8; ++i) mbar_init(&sh.bars[kBarComb + i], 64);
     mbar_init(&sh.bars[kBarDrain], 1);
     *sh.abort_flag = 0;
     fence_mbarrier_init_cluster();
@@ -559,7 +690,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (cta == 0 && it.t == 0 && (beg < 0 || end < beg || end > p.max_pages))
       raise_status(p.status, DCP_STATUS_BAD_SPLIT);
   }
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tmem_alloc(sh.tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -569,17 +700,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *sh.tmem_slot;
 
-  if (warp < 4) {
-    run_softmax<kFp8>(p, sh, it, cta, tbase, tid);
-  } else if (warp < 8) {
-    run_producer<kFp8>(p, sh, it, cta, tid - 128);
-  } else if (tid == 256) {
-    run_mma<kFp8>(p, sh, it, cta, tbase);
+  if (warp < kSoftWarps) {
+    if (cta == 0) run_softmax<kFp8, 4>(p, sh, it, tbase, tid);
+    else run_softmax<kFp8, 5>(p, sh, it, tbase, tid);
+  } else if (warp < kMmaWarp) {
+    if (cta == 0) Producer<kFp8, 4>(p, sh, it, tid - kProdWarp0 * 32).run();
+    else Producer<kFp8, 5>(p, sh, it, tid - kProdWarp0 * 32).run();
+  } else if (tid == kMmaWarp * 32) {
+    if (cta == 0) run_mma<kFp8, 4>(p, sh, it, tbase);
+    else run_mma<kFp8, 5>(p, sh, it, tbase);
   }
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // the peer no longer touches this CTA's shared memory
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }

@@ -22,14 +22,27 @@ def num_sms(device=None) -> int:
 
 def choose_num_splits(batch: int, qlen: int, num_heads: int, num_ranks: int,
                       max_local_len: int, block_size: int, sms: int = 152) -> int:
-    """Static split count: enough CTAs to fill every SM twice over, while each
-    split keeps at least four subpages of work at the static bound."""
+    """Static split count for the partial kernel.
+
+    Each work item (rank, sequence, split, 128-row tile) runs on a cluster of two
+    CTAs, one CTA per SM, so ``sms // 2`` items run at once. Pick the split count
+    whose item count fills the last wave best (within 3 % of the best, the
+    smallest such count), keeping at least eight subpages of work per split at
+    the static bound. Uses only static sizes, so the choice is graph-safe.
+    """
     P = B.dcp_mla_subpage_size(block_size)
     pages = max(1, math.ceil(max_local_len / P))
     tiles = math.ceil(qlen * num_heads / 128)
-    ctas = max(1, batch * num_ranks * tiles)
-    want = max(1, math.ceil(2 * sms / ctas))
-    return int(max(1, min(want, pages // 4 if pages >= 4 else 1, 256)))
+    base = max(1, batch * num_ranks * tiles)
+    slots = max(1, sms // 2)
+    max_ns = max(1, min(64, pages // 8))
+    best = []
+    for ns in range(1, max_ns + 1):
+        items = base * ns
+        eff = items / (math.ceil(items / slots) * slots)
+        best.append((eff, ns))
+    top = max(e for e, _ in best)
+    return int(min(ns for e, ns in best if e >= 0.97 * top))
 
 
 def make_dims(*, batch, qlen, num_heads, dcp, interleave, block_size, max_blocks_per_seq,
