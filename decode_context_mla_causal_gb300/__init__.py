@@ -16,7 +16,9 @@ from .binding import (  # noqa: F401
 )
 from .step import VerifyStep, choose_num_splits, make_dims, num_sms  # noqa: F401
 
-#: Arithmetic type of the hot path (reported by bench.py).
-COMPUTE_DTYPE = "f32"
+#: Arithmetic type of the hot path (reported by bench.py): 16-bit tensor-core
+#: contractions (f16 for the FP8 cache, bf16 for the BF16 cache), fp32 accumulation,
+#: fp32 softmax statistics.
+COMPUTE_DTYPE = "f16/bf16 MMA, f32 accumulate"
 
 load()

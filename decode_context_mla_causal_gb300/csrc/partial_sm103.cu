@@ -27,24 +27,34 @@
 //     normalises its own half of O by its own l.
 //   * CTA c stages dims [256c, 256c + 256 + 64c) of every token: its q.k slice,
 //     which also holds its value slice.
+//   * A tcgen05.mma of M=128 costs about 190 cycles of issue latency per thread
+//     whatever its N (measured), so N=64 score MMAs only reach full rate when
+//     several warps issue independent chains. The q.k contraction is therefore
+//     split into two chains with their own accumulators, issued by two warps:
+//     chain A (dims atoms 0-1, q operand in TMEM) and chain B (atoms 2.., q
+//     operand in shared memory); the softmax adds the two partial scores.
+//   * The factor exchange runs one tile behind: iteration i loads the scores of
+//     tile i and sends its factors, then finishes tile i-1 with the factors the
+//     peer sent an iteration earlier, so the exchange latency overlaps work.
 //
-// Per CTA (416 threads):
+// Per CTA (448 threads):
 //   warps 0-7   softmax: warp w owns rows 32*(w%4) .. +31 (TMEM lane quarter)
-//               and token half w/4 of every 64-token tile; Q into TMEM, factor
-//               exchange (double-buffered slots), lazy online softmax, P
-//               (16-bit) into TMEM, epilogue for O columns [128*(w/4), +128).
+//               and token half w/4 of every 64-token tile; Q (TMEM + smem),
+//               factor exchange (double-buffered slots), lazy online softmax,
+//               P (16-bit) into TMEM, epilogue for O columns [128*(w/4), +128).
 //   warps 8-11  KV producers: 16-byte loads of the paged cache rows (subpage ids
 //               from the metadata, bounds-checked, two tiles in flight), FP8
 //               E4M3 -> f16 conversion, stores into 128-byte-swizzled K-major
-//               tiles of a 4-stage ring.
-//   warp 12     TMEM allocation and the single MMA-issuing thread:
-//               S  = Q[tmem] . K_tile^T        (M=128, N=64,  K=16 per MMA)
-//               O += P[tmem] . V_tile          (M=128, N=256, V read MN-major
-//                                               from the same swizzled tile)
-// TMEM columns: O [0,256), S [256,320), P [320,352), Q [352, 352 + 32*atoms).
-// The FP8-cache path computes in f16 (E4M3 -> f16 is exact; q is BF16 -> f16,
-// exact in f16's normal range; |q| > 65504 sets DCP_STATUS_Q_RANGE); the BF16
-// cache path computes in bf16. Accumulation is fp32 throughout.
+//               tiles of a 3-stage ring.
+//   warp 12     TMEM allocation; one thread issues chain A of S(i)
+//               (Q[tmem] . K_tile^T, M=128 N=64) and O += P[tmem] . V_tile
+//               (M=128, N=256, V read MN-major from the same swizzled tile).
+//   warp 13     one thread issues chain B of S(i) (Q[smem] . K_tile^T).
+// TMEM columns: O [0,256), S_a [256,320), S_b [320,384), P [384,416),
+// Q chain A [416,480). The FP8-cache path computes in f16 (E4M3 -> f16 is exact;
+// q is BF16 -> f16, exact in f16's normal range; |q| > 65504 sets
+// DCP_STATUS_Q_RANGE); the BF16-cache path computes in bf16. Accumulation is
+// fp32 throughout.
 //
 // Every wait is bounded (DCP_STATUS_TIMEOUT and an orderly exit: all roles stop,
 // in-flight MMAs are drained, TMEM is freed). Waiting threads sleep in
@@ -63,10 +73,15 @@ using namespace sm103;
 
 constexpr int kTileN = 64;     // tokens per KV tile
 constexpr int kRows = 128;     // query rows per tile (MMA M)
-constexpr int kStages = 4;     // KV ring depth
+constexpr int kStages = 3;     // KV ring depth
 constexpr int kMaxAtoms = 5;   // 64-dim swizzle atoms staged per CTA (CTA1: 320 dims)
 constexpr int kAtomBytes = kTileN * 128;
 constexpr int kStageBytes = kMaxAtoms * kAtomBytes;
+constexpr int kQAtomBytes = kRows * 128;       // one 64-dim atom of Q (128 rows)
+constexpr int kChainAAtoms = 2;                // q.k atoms 0..1 form chain A, the rest chain B
+constexpr int kQTmemAtoms = 3;                 // q atoms 0..2 live in TMEM, 3.. in smem
+constexpr int kQSmemBytes = (kMaxAtoms - kQTmemAtoms) * kQAtomBytes;
+constexpr int kEPrevBytes = 2 * kTileN / 2 * kRows * 4;  // own fp32 factors [half][32][row]
 // factor exchange slot: E as f16 [half 2][group 4][row 128][8 values], m as f32 [half][row]
 constexpr int kXchEBytes = 2 * 4 * kRows * 16;
 constexpr int kXchSlotBytes = kXchEBytes + 2 * kRows * 4;
@@ -74,33 +89,38 @@ constexpr int kXchSlots = 2;
 constexpr int kCombBytes = 2 * 2 * kRows * 4;  // [parity][half][row] f32 for the half combine
 constexpr int kSoftWarps = 8;
 constexpr int kProdWarp0 = 8;
-constexpr int kMmaWarp = 12;
-constexpr int kThreads = 13 * 32;
-constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
+constexpr int kMmaWarpA = 12;
+constexpr int kMmaWarpB = 13;
+constexpr int kThreads = 14 * 32;
+constexpr uint32_t kColO = 0, kColSa = 256, kColSb = 320, kColP = 384, kColQ = 416;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // P may grow to 2^8 before O is rescaled
-constexpr float kFactorScale = 16384.0f;   // 2^14: keeps E down to 2^-28 normal in f16
+constexpr float kFactorLog2 = 14.0f;       // factors carry 2^14: E down to 2^-28 stays normal in f16
 constexpr uint64_t kTimeoutNs = 4000000000ull;
+constexpr uint64_t kPollNs = 20000;  // poll this long before sleeping in a wait
 constexpr float kLog2e = 1.4426950408889634f;
 
 // barrier slots
 enum {
   kBarKvFull = 0,
-  kBarKvEmpty = kBarKvFull + kStages,
-  kBarSFull = kBarKvEmpty + kStages,
+  kBarKvEmpty = kBarKvFull + kStages,  // count 2: PV (chain A thread) and chain B
+  kBarSFullA = kBarKvEmpty + kStages,
+  kBarSFullB,
   kBarSFree,
   kBarPFull,
   kBarODone,
   kBarQFull,
-  kBarXFull,                     // [2] the peer's factors are in my slot
+  kBarXFull,                          // [2] the peer's factors are in my slot
   kBarXFree = kBarXFull + kXchSlots,  // [2] the peer consumed what I wrote into its slot
-  kBarComb = kBarXFree + kXchSlots,  // [4 lane quarters][2 parities] half-combine, count 64
-  kBarDrain = kBarComb + 8,
+  kBarComb = kBarXFree + kXchSlots,   // [4 lane quarters][2 parities] half-combine, count 64
+  kBarDrainA = kBarComb + 8,
+  kBarDrainB,
   kNumBars
 };
 
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes +
-                              kXchSlots * kXchSlotBytes + kCombBytes + kNumBars * 8 + 16;
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kQSmemBytes +
+                              kXchSlots * kXchSlotBytes + kCombBytes + kEPrevBytes +
+                              kNumBars * 8 + 16;
 
 struct Params {
   const uint16_t* q;
@@ -121,8 +141,10 @@ struct Params {
 
 struct Shared {
   uint8_t* stages;
+  uint8_t* qs;   // Q atoms kQTmemAtoms.. (shared-memory operand of chain B)
   uint8_t* xch;  // kXchSlots slots
   float* comb;
+  float* eprev;  // own factors of the tile awaiting the peer's
   uint64_t* bars;
   uint32_t* tmem_slot;
   int* abort_flag;
@@ -133,29 +155,37 @@ __device__ __forceinline__ Shared carve(unsigned char* raw) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   s.stages = base;
-  s.xch = base + kStages * kStageBytes;
+  s.qs = base + kStages * kStageBytes;
+  s.xch = s.qs + kQSmemBytes;
   s.comb = reinterpret_cast<float*>(s.xch + kXchSlots * kXchSlotBytes);
-  s.bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.comb) + kCombBytes);
+  s.eprev = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s.comb) + kCombBytes);
+  s.bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.eprev) + kEPrevBytes);
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + kNumBars);
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
   return s;
 }
 
-// Bounded wait on an mbarrier phase. The slow path sleeps in try_wait (with a
-// suspend-time hint) instead of spinning, gives up after kTimeoutNs (raising the
-// abort flag and DCP_STATUS_TIMEOUT), and returns false at once when another
-// thread of the CTA has already aborted.
+// Bounded wait on an mbarrier phase. The slow path polls try_wait for a few
+// microseconds (a suspended waiter was measured to wake up to ~0.5 us late),
+// then sleeps in try_wait with a suspend-time hint; it gives up after
+// kTimeoutNs (raising the abort flag and DCP_STATUS_TIMEOUT), and returns false
+// at once when another thread of the CTA has already aborted.
 __device__ __noinline__ bool wait_phase_slow(uint32_t a, uint32_t parity, int* abort_flag,
                                              uint32_t* status, bool cluster_acquire) {
   const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    if (cluster_acquire ? mbar_wait_sleep_cluster(a, parity) : mbar_wait_sleep(a, parity))
-      return true;
-    if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
-    if (globaltimer_ns() - t0 > kTimeoutNs) {
-      *reinterpret_cast<volatile int*>(abort_flag) = 1;
-      raise_status(status, DCP_STATUS_TIMEOUT);
-      return false;
+  for (uint32_t it = 1;; ++it) {
+    if (cluster_acquire ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
+    if ((it & 31u) == 0) {
+      const uint64_t dt = globaltimer_ns() - t0;
+      if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
+      if (dt > kTimeoutNs) {
+        *reinterpret_cast<volatile int*>(abort_flag) = 1;
+        raise_status(status, DCP_STATUS_TIMEOUT);
+        return false;
+      }
+      if (dt > kPollNs &&
+          (cluster_acquire ? mbar_wait_sleep_cluster(a, parity) : mbar_wait_sleep(a, parity)))
+        return true;
     }
   }
 }
@@ -214,36 +244,50 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
 }
 
 // ----------------------------------------------------------------- producers
-// One work unit is one 16-byte global load. FP8: unit u -> quarter u&3 (16 dims,
-// two 16-byte f16 chunks), token (u>>2)&63, atom u>>8. BF16: unit u -> chunk u&7
-// (8 dims), token (u>>3)&63, atom u>>9. A warp thus covers 8 (FP8) or 4 (BF16)
-// consecutive tokens of one atom: 64-byte (or 128-byte) contiguous global reads
-// per token, and shared stores that fill whole 128-byte swizzled rows (no bank
-// conflicts beyond the four wavefronts a 512-byte warp store needs).
+// Each producer thread owns fixed tokens of every tile and one 16-byte column
+// of every atom: FP8 -> tokens tk0 and tk0+32 (tk0 = ct/4), 16 dims at
+// quarter ct%4 (two f16 chunks out); BF16 -> tokens tk0 + 16j (tk0 = ct/8),
+// 8 dims at chunk ct%8. A warp then covers 8 (or 4) consecutive tokens of one
+// atom: contiguous global reads per token and shared stores that fill whole
+// 128-byte swizzled rows. Row addresses are formed once per token per tile, so
+// the unrolled load/store code is short (it competes for instruction cache
+// with the softmax warps of the same SM).
 template <bool kFp8, int kAtoms>
 struct Producer {
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kD0 = 256 * (kAtoms - 4);  // first staged dim: 0 (CTA0) or 256 (CTA1)
-  static constexpr int kUnitsPerAtom = kFp8 ? 256 : 512;
-  static constexpr int kLoads = kAtoms * kUnitsPerAtom / 128;
+  static constexpr int kToks = kFp8 ? 2 : 4;       // tokens per thread per tile
+  static constexpr int kTokStride = kFp8 ? 32 : 16;
+  static constexpr int kLoads = kAtoms * kToks;
 
   const Params& p;
   const Shared& sh;
   const Item& it;
-  int ct, lg_sub;
+  int lg_sub, tk0;
+  uint32_t col;   // byte offset of this thread's 16 bytes inside an atom row (global)
+  uint32_t soff0; // swizzled smem offset of this thread's first output chunk, token tk0
   int64_t pool_pages;
   const uint8_t* pool;
   const int32_t* pages;
   bool big_pages, bad_page;
 
-  __device__ __forceinline__ Producer(const Params& p_, const Shared& sh_, const Item& it_, int ct_)
-      : p(p_), sh(sh_), it(it_), ct(ct_) {
+  __device__ __forceinline__ Producer(const Params& p_, const Shared& sh_, const Item& it_, int ct)
+      : p(p_), sh(sh_), it(it_) {
     lg_sub = __ffs(p.subpage) - 1;
     pool_pages = p.pool_rows >> lg_sub;
     pool = p.kv + (int64_t)it.k * p.pool_rows * kDqk * kElem;
     pages = p.page_ids + ((int64_t)it.k * p.batch + it.b) * p.max_pages;
     big_pages = p.subpage >= kTileN;  // then a tile lies inside one subpage
     bad_page = false;
+    if (kFp8) {
+      tk0 = ct >> 2;
+      col = (ct & 3) * 16;
+      soff0 = sw128_offset(tk0, 2 * (ct & 3));  // chunk 2q; chunk 2q+1 is 16 bytes away (xor)
+    } else {
+      tk0 = ct >> 3;
+      col = (ct & 7) * 16;
+      soff0 = sw128_offset(tk0, ct & 7);
+    }
   }
 
   __device__ __forceinline__ int32_t tile_page(int i) const {
@@ -252,30 +296,28 @@ struct Producer {
   }
 
   __device__ __forceinline__ void load(int i, int32_t pg_tile, uint4 (&v)[kLoads]) {
-    const int tok0 = it.t_start + i * kTileN;
+    const int tok0 = it.t_start + i * kTileN + tk0;
+    const uint8_t* rp[kToks];
 #pragma unroll
-    for (int l = 0; l < kLoads; ++l) {
-      const int u = l * 128 + ct;
-      int tk, off;
-      if (kFp8) {
-        tk = (u >> 2) & 63;
-        off = kD0 + (u >> 8) * 64 + (u & 3) * 16;
-      } else {
-        tk = (u >> 3) & 63;
-        off = (kD0 + (u >> 9) * 64 + (u & 7) * 8) * 2;
-      }
-      const int li = tok0 + tk;
-      v[l] = make_uint4(0u, 0u, 0u, 0u);
+    for (int j = 0; j < kToks; ++j) {
+      const int li = tok0 + j * kTokStride;
+      rp[j] = nullptr;
       if (li < it.t_end) {
         const int32_t pg = big_pages ? pg_tile : __ldg(pages + (li >> lg_sub));
         if (pg >= 0 && pg < pool_pages) {
           const int64_t row = ((int64_t)pg << lg_sub) + (li & (p.subpage - 1));
-          v[l] = __ldg(reinterpret_cast<const uint4*>(pool + row * (kDqk * kElem) + off));
+          rp[j] = pool + row * (kDqk * kElem) + kD0 * kElem + col;
         } else {
           bad_page = true;
         }
       }
     }
+#pragma unroll
+    for (int a = 0; a < kAtoms; ++a)
+#pragma unroll
+      for (int j = 0; j < kToks; ++j)
+        v[a * kToks + j] = rp[j] ? __ldg(reinterpret_cast<const uint4*>(rp[j] + a * 64 * kElem))
+                                 : make_uint4(0u, 0u, 0u, 0u);
   }
 
   __device__ __forceinline__ bool store(int i, const uint4 (&v)[kLoads]) {
@@ -283,27 +325,29 @@ struct Producer {
     if (i >= kStages && !wait_phase(&sh.bars[kBarKvEmpty + st], ((i / kStages) - 1) & 1,
                                     sh.abort_flag, p.status, false))
       return false;
-    uint8_t* stage = sh.stages + st * kStageBytes;
+    uint8_t* base = sh.stages + st * kStageBytes + soff0;
 #pragma unroll
-    for (int l = 0; l < kLoads; ++l) {
-      const int u = l * 128 + ct;
-      if (kFp8) {
-        const int qq = u & 3, tk = (u >> 2) & 63, a = u >> 8;
-        uint4 lo, hi;
-        lo.x = e4m3x2_to_f16x2(v[l].x);
-        lo.y = e4m3x2_to_f16x2(v[l].x >> 16);
-        lo.z = e4m3x2_to_f16x2(v[l].y);
-        lo.w = e4m3x2_to_f16x2(v[l].y >> 16);
-        hi.x = e4m3x2_to_f16x2(v[l].z);
-        hi.y = e4m3x2_to_f16x2(v[l].z >> 16);
-        hi.z = e4m3x2_to_f16x2(v[l].w);
-        hi.w = e4m3x2_to_f16x2(v[l].w >> 16);
-        uint8_t* at = stage + a * kAtomBytes;
-        *reinterpret_cast<uint4*>(at + sw128_offset(tk, 2 * qq)) = lo;
-        *reinterpret_cast<uint4*>(at + sw128_offset(tk, 2 * qq + 1)) = hi;
-      } else {
-        const int ch = u & 7, tk = (u >> 3) & 63, a = u >> 9;
-        *reinterpret_cast<uint4*>(stage + a * kAtomBytes + sw128_offset(tk, ch)) = v[l];
+    for (int a = 0; a < kAtoms; ++a) {
+#pragma unroll
+      for (int j = 0; j < kToks; ++j) {
+        uint8_t* dst = base + a * kAtomBytes + j * kTokStride * 128;
+        const uint4 x = v[a * kToks + j];
+        if (kFp8) {
+          uint4 lo, hi;
+          lo.x = e4m3x2_to_f16x2(x.x);
+          lo.y = e4m3x2_to_f16x2(x.x >> 16);
+          lo.z = e4m3x2_to_f16x2(x.y);
+          lo.w = e4m3x2_to_f16x2(x.y >> 16);
+          hi.x = e4m3x2_to_f16x2(x.z);
+          hi.y = e4m3x2_to_f16x2(x.z >> 16);
+          hi.z = e4m3x2_to_f16x2(x.w);
+          hi.w = e4m3x2_to_f16x2(x.w >> 16);
+          *reinterpret_cast<uint4*>(dst) = lo;
+          // chunk 2q+1 = (2q ^ (tk & 7)) ^ 1 within the row: 16 bytes further or back
+          *reinterpret_cast<uint4*>(reinterpret_cast<uintptr_t>(dst) ^ 16u) = hi;
+        } else {
+          *reinterpret_cast<uint4*>(dst) = x;
+        }
       }
     }
     fence_proxy_async_smem();
@@ -312,21 +356,21 @@ struct Producer {
   }
 
   // FP8: two register buffers, so tile i+1's loads are in flight while tile i is
-  // converted and stored; tile pages are read two tiles ahead. BF16 (twice the
-  // registers per tile): one buffer.
+  // converted and stored; tile pages are read one tile ahead. BF16 (twice the
+  // registers per tile): one buffer. One call site each keeps the code small.
   __device__ __forceinline__ void run() {
     const int n = it.n_tiles;
     if (kFp8) {
       uint4 va[kLoads], vb[kLoads];
-      int32_t pg1 = tile_page(1);
+      int32_t pg_next = tile_page(1);
       load(0, tile_page(0), va);
-      for (int i = 0; i < n; i += 2) {
-        const int32_t pg2 = tile_page(i + 2);
-        if (i + 1 < n) load(i + 1, pg1, vb);
-        if (!store(i, va) || i + 1 >= n) break;
-        pg1 = tile_page(i + 3);
-        if (i + 2 < n) load(i + 2, pg2, va);
-        if (!store(i + 1, vb)) break;
+      for (int i = 0; i < n; ++i) {
+        const int32_t pg = pg_next;
+        pg_next = tile_page(i + 2);
+        if (i + 1 < n) load(i + 1, pg, vb);
+        if (!store(i, va)) break;
+#pragma unroll
+        for (int l = 0; l < kLoads; ++l) va[l] = vb[l];
       }
     } else {
       uint4 v[kLoads];
@@ -339,11 +383,13 @@ struct Producer {
   }
 };
 
-// ----------------------------------------------------------------- MMA issuer
+// ----------------------------------------------------------------- MMA issuers
+// Chain A of every score tile plus every P.V; PV(j) is issued two tiles late
+// (after the score chain of tile j+2), because P(j) is finished one softmax
+// iteration after S(j) is read.
 template <bool kFp8, int kAtoms>
-__device__ __forceinline__ void run_mma(const Params& p, const Shared& sh, const Item& it,
-                                        uint32_t tbase) {
-  constexpr int n_atoms = kAtoms;
+__device__ __forceinline__ void run_mma_a(const Params& p, const Shared& sh, const Item& it,
+                                          uint32_t tbase) {
   const uint32_t idq = idesc_f16(kRows, kTileN, !kFp8, false);
   const uint32_t idp = idesc_f16(kRows, 256, !kFp8, true);
   const uint32_t stage0 = smem_u32(sh.stages);
@@ -362,277 +408,90 @@ __device__ __forceinline__ void run_mma(const Params& p, const Shared& sh, const
     tc_commit(&sh.bars[kBarKvEmpty + (j % kStages)]);
     return true;
   };
-  for (int i = 0; ok && i < it.n_tiles; ++i) {
-    const int st = i % kStages;
-    if (!wait_phase(&sh.bars[kBarKvFull + st], (i / kStages) & 1, sh.abort_flag, p.status, false))
-      break;
-    if (i >= 1 && !wait_phase(&sh.bars[kBarSFree], (i - 1) & 1, sh.abort_flag, p.status, false))
-      break;
-    tc_fence_after();
-    const uint32_t sa = stage0 + st * kStageBytes;
+  const int n = it.n_tiles;
+  for (int i = 0; ok && i < n + 2; ++i) {
+    if (i < n) {
+      const int st = i % kStages;
+      if (!wait_phase(&sh.bars[kBarKvFull + st], (i / kStages) & 1, sh.abort_flag, p.status,
+                      false))
+        break;
+      if (i >= 1 && !wait_phase(&sh.bars[kBarSFree], (i - 1) & 1, sh.abort_flag, p.status, false))
+        break;
+      tc_fence_after();
+      const uint32_t sa = stage0 + st * kStageBytes;
 #pragma unroll
-    for (int kk = 0; kk < n_atoms * 4; ++kk) {
-      const uint64_t d = smem_desc_sw128(sa + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024);
-      mma_f16_ts(tbase + kColS, tbase + kColQ + 8 * kk, d, idq, kk > 0 ? 1u : 0u);
+      for (int kk = 0; kk < 4 * kChainAAtoms; ++kk) {
+        const uint64_t d = smem_desc_sw128(sa + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024);
+        mma_f16_ts(tbase + kColSa, tbase + kColQ + 8 * kk, d, idq, kk > 0 ? 1u : 0u);
+      }
+      tc_commit(&sh.bars[kBarSFullA]);
     }
-    tc_commit(&sh.bars[kBarSFull]);
-    if (i >= 1 && !issue_pv(i - 1)) {
-      ok = false;
-      break;
+    if (i >= 2 && !issue_pv(i - 2)) ok = false;
+  }
+  // drain: every MMA issued above has completed before TMEM can be released
+  tc_commit(&sh.bars[kBarDrainA]);
+  int never = 0;
+  wait_phase(&sh.bars[kBarDrainA], 0, &never, p.status, false);
+}
+
+// Chain B of every score tile (q operand from shared memory).
+template <bool kFp8, int kAtoms>
+__device__ __forceinline__ void run_mma_b(const Params& p, const Shared& sh, const Item& it,
+                                          uint32_t tbase) {
+  const uint32_t idq = idesc_f16(kRows, kTileN, !kFp8, false);
+  const uint32_t stage0 = smem_u32(sh.stages);
+  const uint32_t q0 = smem_u32(sh.qs);
+  if (wait_phase(&sh.bars[kBarQFull], 0, sh.abort_flag, p.status, false)) {
+    tc_fence_after();
+    for (int i = 0; i < it.n_tiles; ++i) {
+      const int st = i % kStages;
+      if (!wait_phase(&sh.bars[kBarKvFull + st], (i / kStages) & 1, sh.abort_flag, p.status,
+                      false))
+        break;
+      if (i >= 1 && !wait_phase(&sh.bars[kBarSFree], (i - 1) & 1, sh.abort_flag, p.status, false))
+        break;
+      tc_fence_after();
+      const uint32_t sa = stage0 + st * kStageBytes;
+#pragma unroll
+      for (int kk = 4 * kChainAAtoms; kk < 4 * kAtoms; ++kk) {
+        const uint64_t b = smem_desc_sw128(sa + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024);
+        const uint32_t acc = kk > 4 * kChainAAtoms ? 1u : 0u;
+        if ((kk >> 2) < kQTmemAtoms) {
+          mma_f16_ts(tbase + kColSb, tbase + kColQ + 8 * kk, b, idq, acc);
+        } else {
+          const uint64_t a = smem_desc_sw128(
+              q0 + ((kk >> 2) - kQTmemAtoms) * kQAtomBytes + (kk & 3) * 32, 16, 1024);
+          mma_f16_ss(tbase + kColSb, a, b, idq, acc);
+        }
+      }
+      tc_commit(&sh.bars[kBarSFullB]);
+      tc_commit(&sh.bars[kBarKvEmpty + st]);
     }
   }
-  if (ok && it.n_tiles > 0 && !*reinterpret_cast<volatile int*>(sh.abort_flag))
-    issue_pv(it.n_tiles - 1);
-  // drain: every MMA issued above has completed before TMEM can be released
-  tc_commit(&sh.bars[kBarDrain]);
-  int* dummy_abort = sh.abort_flag;
+  tc_commit(&sh.bars[kBarDrainB]);
   int never = 0;
-  wait_phase(&sh.bars[kBarDrain], 0, &never, p.status, false);
-  (void)dummy_abort;
+  wait_phase(&sh.bars[kBarDrainB], 0, &never, p.status, false);
 }
 
 // ----------------------------------------------------------------- softmax
-template <bool kFp8, int kAtoms>
-__device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, const Item& it,
-                                            uint32_t tbase, int tid) {
-  constexpr int cta = kAtoms - 4;
-  constexpr int d0 = 256 * cta;
-  constexpr int kAtomsLo = (kAtoms + 1) / 2;  // Q atoms loaded by half 0
-  const int warp = tid >> 5, lane = tid & 31;
-  const int qw = warp & 3;   // TMEM lane quarter
-  const int h = warp >> 2;   // token half of each tile / O column half
-  const int r = qw * 32 + lane;
-  const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-  const uint32_t tS = tbase + lane_off + kColS + 32 * h;
-  const uint32_t tP = tbase + lane_off + kColP + 16 * h;
-  const uint32_t tO = tbase + lane_off + kColO + 128 * h;
-  const uint32_t tQ = tbase + lane_off + kColQ;
-  const int qrows = p.qlen * p.H;
-  const int R = p.batch * p.qlen;
-  const bool row_ok = r < it.rows_valid;
-  const int qr = it.qr0 + r;
-  const int j = row_ok ? qr / p.H : 0;
-  const int L = row_ok ? p.row_len[(int64_t)it.k * R + (int64_t)it.b * p.qlen + j] : 0;
-  const int row_end = min(L, it.t_end);  // tokens at or past it are invisible to this row
-  const float kv_scale = p.kv_scale ? *p.kv_scale : 1.0f;
-  const float sc = p.softmax_scale * kv_scale * kLog2e;
+// Rare paths live out of line so that the per-tile loop stays small in the
+// instruction cache (it shares the SM with the producer and MMA warps).
 
-  // Q slice -> TMEM (16-bit pairs along the dims, lane = row); half h loads its atoms
-  {
-    const uint16_t* src = p.q + ((int64_t)it.b * qrows + qr) * kDqk + d0;
-    bool q_range = false;
-    const int a0 = h == 0 ? 0 : kAtomsLo;
-    const int a1 = h == 0 ? kAtomsLo : kAtoms;
-#pragma unroll 1
-    for (int a = a0; a < a1; ++a) {
-      uint32_t w[32];
+// O[:, this warp's 128 columns] *= a (per-thread row factor); warp-collective.
+__device__ __noinline__ void rescale_o(uint32_t tO, float a) {
+  for (int c8 = 0; c8 < 8; ++c8) {
+    uint32_t o[16];
+    tmem_ld16(tO + 16 * c8, o);
+    tmem_wait_ld16(o);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (row_ok) v = __ldg(reinterpret_cast<const uint4*>(src + a * 64 + c * 8));
-        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (kFp8) {
-            const float f0 = __uint_as_float(x[e] << 16);
-            const float f1 = __uint_as_float(x[e] & 0xFFFF0000u);
-            q_range |= fabsf(f0) > 65504.f || fabsf(f1) > 65504.f;
-            __half2 hh = __floats2half2_rn(f0, f1);
-            w[c * 4 + e] = *reinterpret_cast<uint32_t*>(&hh);
-          } else {
-            w[c * 4 + e] = x[e];
-          }
-        }
-      }
-      tmem_st32(tQ + 32 * a, w);
-    }
-    tmem_wait_st();
-    if (q_range) raise_status(p.status, DCP_STATUS_Q_RANGE);
-    tc_fence_before();
-    mbar_arrive(&sh.bars[kBarQFull]);
+    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+    tmem_st16(tO + 16 * c8, o);
   }
+}
 
-  const uint32_t peer = cta ^ 1;
-  const uint32_t xch_local = smem_u32(sh.xch);
-  const uint32_t xch_remote = mapa_shared(xch_local, peer);
-  const uint32_t xfull_remote = mapa_shared(smem_u32(&sh.bars[kBarXFull]), peer);
-  const uint32_t xfree_remote = mapa_shared(smem_u32(&sh.bars[kBarXFree]), peer);
-  const int32_t* pages = p.page_ids + ((int64_t)it.k * p.batch + it.b) * p.max_pages;
-  const int lg_sub = __ffs(p.subpage) - 1;
-  const int64_t pool_pages = p.pool_rows >> lg_sub;
-  const bool big_pages = p.subpage >= kTileN;
-  // The two warps sharing rows (w and w^4) combine per-row values through smem,
-  // synchronised by an mbarrier per (lane quarter, parity) with bounded waits.
-  auto pair_sync = [&](int i) -> bool {
-    uint64_t* bar = &sh.bars[kBarComb + qw * 2 + (i & 1)];
-    mbar_arrive(bar);
-    return __all_sync(0xffffffffu, wait_phase(bar, (i >> 1) & 1, sh.abort_flag, p.status, false));
-  };
-
-  // Waits are made warp-uniform: the tcgen05.ld/st that follow are warp-collective.
-  auto wait_warp = [&](int bar, uint32_t parity, bool cluster) -> bool {
-    return __all_sync(0xffffffffu,
-                      wait_phase(&sh.bars[bar], parity, sh.abort_flag, p.status, cluster));
-  };
-  float M = -INFINITY;  // running reference (log2 units), same in both CTAs
-  float l_half = 0.f;   // sum of this half's weights
-  bool ok = true;
-  int32_t pg_next = (big_pages && it.n_tiles > 0) ? __ldg(pages + (it.t_start >> lg_sub)) : 0;
-  for (int i = 0; i < it.n_tiles; ++i) {
-    const int tok0 = it.t_start + i * kTileN;
-    const int32_t pg_tile = pg_next;
-    if (!wait_warp(kBarSFull, i & 1, false)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-    uint32_t s[32];
-    tmem_ld32(tS, s);
-    tmem_wait_ld(s);
-    tc_fence_before();
-    mbar_arrive(&sh.bars[kBarSFree]);
-
-    // visible tokens of this row in this half: [tok0 + 32h, row_end), pages valid
-    const int cnt = max(0, min(32, row_end - tok0 - 32 * h));
-    uint32_t vis = cnt >= 32 ? 0xFFFFFFFFu : ((1u << cnt) - 1u);
-    if (big_pages) {
-      if (pg_tile < 0 || pg_tile >= pool_pages) vis = 0;
-    } else if (vis) {
-      const int first = (tok0 + 32 * h) >> lg_sub;
-      const int last = (tok0 + 32 * h + cnt - 1) >> lg_sub;
-      for (int q = first; q <= last; ++q) {
-        const int32_t pg = pages[q];
-        if (pg < 0 || pg >= pool_pages) {
-          const int lo = max(0, (q << lg_sub) - (tok0 + 32 * h));
-          const int hi = min(32, ((q + 1) << lg_sub) - (tok0 + 32 * h));
-          const uint32_t m = (hi - lo >= 32) ? 0xFFFFFFFFu : (((1u << (hi - lo)) - 1u) << lo);
-          vis &= ~m;
-        }
-      }
-    }
-    float x[32];
-    float m_own = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      x[c] = __uint_as_float(s[c]) * sc;
-      if ((vis >> c) & 1u) m_own = fmaxf(m_own, x[c]);
-    }
-    // own factors E = 2^(x - m_own) (fp32, kept), sent as f16 * 2^14
-    uint32_t e16[16];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) x[c] = ((vis >> c) & 1u) ? fast_exp2(x[c] - m_own) : 0.f;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      __half2 hh = __floats2half2_rn(x[2 * c] * kFactorScale, x[2 * c + 1] * kFactorScale);
-      e16[c] = *reinterpret_cast<uint32_t*>(&hh);
-    }
-    // send to the peer's slot (i & 1); it must have consumed what it held two tiles ago
-    const int slot = i & 1;
-    if (i >= 2 && !wait_warp(kBarXFree + slot, ((i >> 1) - 1) & 1, true)) {
-      ok = false;
-      break;
-    }
-    {
-      const uint32_t dst = xch_remote + slot * kXchSlotBytes;
-#pragma unroll
-      for (int g = 0; g < 4; ++g)
-        st_cluster_v4(dst + (uint32_t)(((h * 4 + g) * kRows + r) * 16), e16[4 * g],
-                      e16[4 * g + 1], e16[4 * g + 2], e16[4 * g + 3]);
-      const uint32_t mdst = dst + kXchEBytes + (uint32_t)((h * kRows + r) * 4);
-      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(mdst), "f"(m_own) : "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(xfull_remote + 8 * slot);  // releases the warp's stores
-    }
-    if (!wait_warp(kBarXFull + slot, (i >> 1) & 1, true)) {
-      ok = false;
-      break;
-    }
-    uint4 pe[4];
-    float m_peer;
-    {
-      const uint8_t* src = sh.xch + slot * kXchSlotBytes;
-#pragma unroll
-      for (int g = 0; g < 4; ++g)
-        pe[g] = *reinterpret_cast<const uint4*>(src + ((h * 4 + g) * kRows + r) * 16);
-      m_peer = *reinterpret_cast<const float*>(src + kXchEBytes + (h * kRows + r) * 4);
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(xfree_remote + 8 * slot);
-    }
-    // tile bound of the row (max over both halves of m_own + m_peer)
-    const float ub_h = (m_own == -INFINITY || m_peer == -INFINITY) ? -INFINITY : m_own + m_peer;
-    float* comb = sh.comb + (i & 1) * 2 * kRows;
-    comb[h * kRows + r] = ub_h;
-    if (!pair_sync(i)) {
-      ok = false;
-      break;
-    }
-    const float ub = fmaxf(ub_h, comb[(h ^ 1) * kRows + r]);
-    const bool need = ub != -INFINITY && (M == -INFINITY || ub > M + kRescaleThreshold);
-    float alpha = 1.f;
-    if (need) {
-      alpha = M == -INFINITY ? 0.f : fast_exp2(M - ub);
-      l_half *= alpha;
-      M = ub;
-    }
-    // p = E_own * E_peer * 2^(m_own + m_peer - M)  (E_peer carries 2^14)
-    const float f = ub_h == -INFINITY ? 0.f : fast_exp2(ub_h - M) * (1.0f / kFactorScale);
-    uint32_t pk[16];
-    float lsum = 0.f;
-    const uint32_t pw[16] = {pe[0].x, pe[0].y, pe[0].z, pe[0].w, pe[1].x, pe[1].y,
-                             pe[1].z, pe[1].w, pe[2].x, pe[2].y, pe[2].z, pe[2].w,
-                             pe[3].x, pe[3].y, pe[3].z, pe[3].w};
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const float2 ep = __half22float2(*reinterpret_cast<const __half2*>(&pw[c]));
-      const float p0 = x[2 * c] * ep.x * f;
-      const float p1 = x[2 * c + 1] * ep.y * f;
-      // l sums the fp32 weights; the P.V contraction uses P rounded to 16 bits
-      lsum += p0 + p1;
-      if (kFp8) {
-        __half2 hh = __floats2half2_rn(p0, p1);
-        pk[c] = *reinterpret_cast<uint32_t*>(&hh);
-      } else {
-        __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
-        pk[c] = *reinterpret_cast<uint32_t*>(&hh);
-      }
-    }
-    l_half += lsum;
-    if (big_pages && i + 1 < it.n_tiles) pg_next = __ldg(pages + ((tok0 + kTileN) >> lg_sub));
-    // PV(i-1) done: P buffer is free and O is stable
-    if (i >= 1 && !wait_warp(kBarODone, (i - 1) & 1, false)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-    if (i >= 1 && __any_sync(0xffffffffu, need)) {
-      const float a = need ? alpha : 1.f;
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t o[32];
-        tmem_ld32(tO + 32 * c4, o);
-        tmem_wait_ld(o);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
-        tmem_st32(tO + 32 * c4, o);
-      }
-    }
-    tmem_st16(tP, pk);
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(&sh.bars[kBarPFull]);
-  }
-
-  // epilogue: both halves' l, then this warp's 128 O columns of its rows
-  const bool have_o = __all_sync(0xffffffffu, ok) && it.n_tiles > 0 &&
-                      wait_warp(kBarODone, (it.n_tiles - 1) & 1, false);
-  tc_fence_after();
-  float* comb = sh.comb + (it.n_tiles & 1) * 2 * kRows;
-  comb[h * kRows + r] = l_half;
-  const bool paired = pair_sync(it.n_tiles);
-  const float l_run = l_half + comb[(h ^ 1) * kRows + r];
-  const int64_t rh = (int64_t)it.b * qrows + qr;
-  const int64_t base = ((int64_t)it.k * p.num_splits + it.s) * ((int64_t)R * p.H) + rh;
-  const float inv = (paired && l_run > 0.f) ? kv_scale / l_run : 0.f;
-  float* dst = p.part_o + base * kDv + 256 * cta + 128 * h;
+// Stores this warp's rows of the normalised partial output (128 columns).
+__device__ __noinline__ void store_o(uint32_t tO, bool have_o, bool row_ok, float inv,
+                                     float* dst) {
   for (int c4 = 0; c4 < 4; ++c4) {
     uint32_t o[32];
     if (have_o) {
@@ -651,6 +510,301 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
       }
     }
   }
+}
+
+// Q slice of one row: atoms 0..kQTmemAtoms-1 -> TMEM, the rest -> smem (swizzled
+// K-major); half 0 loads atoms 0-1, half 1 the rest. Returns true if some |q|
+// exceeds the f16 range on the FP8 path.
+template <bool kFp8, int kAtoms>
+__device__ __noinline__ bool load_q(const uint16_t* src, bool row_ok, int h, int r, uint32_t tQ,
+                                    uint8_t* qs) {
+  bool q_range = false;
+  const int a0 = h == 0 ? 0 : 2;
+  const int a1 = h == 0 ? 2 : kAtoms;
+  for (int a = a0; a < a1; ++a) {
+    uint32_t w[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (row_ok) v = __ldg(reinterpret_cast<const uint4*>(src + a * 64 + c * 8));
+      const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (kFp8) {
+          const float f0 = __uint_as_float(x[e] << 16);
+          const float f1 = __uint_as_float(x[e] & 0xFFFF0000u);
+          q_range |= fabsf(f0) > 65504.f || fabsf(f1) > 65504.f;
+          __half2 hh = __floats2half2_rn(f0, f1);
+          w[c * 4 + e] = *reinterpret_cast<uint32_t*>(&hh);
+        } else {
+          w[c * 4 + e] = x[e];
+        }
+      }
+    }
+    if (a < kQTmemAtoms) {
+      tmem_st32(tQ + 32 * a, w);
+    } else {
+      uint8_t* at = qs + (a - kQTmemAtoms) * kQAtomBytes;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(at + sw128_offset(r, c)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    }
+  }
+  tmem_wait_st();
+  return q_range;
+}
+
+template <bool kFp8, int kAtoms>
+__device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, const Item& it,
+                                            uint32_t tbase, int tid) {
+  constexpr int cta = kAtoms - 4;
+  constexpr int d0 = 256 * cta;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int qw = warp & 3;   // TMEM lane quarter
+  const int h = warp >> 2;   // token half of each tile / O column half
+  const int r = qw * 32 + lane;
+  const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+  const uint32_t tSa = tbase + lane_off + kColSa + 32 * h;
+  const uint32_t tSb = tbase + lane_off + kColSb + 32 * h;
+  const uint32_t tP = tbase + lane_off + kColP + 16 * h;
+  const uint32_t tO = tbase + lane_off + kColO + 128 * h;
+  const uint32_t tQ = tbase + lane_off + kColQ;
+  const int qrows = p.qlen * p.H;
+  const int R = p.batch * p.qlen;
+  const bool row_ok = r < it.rows_valid;
+  const int qr = it.qr0 + r;
+  const int j = row_ok ? qr / p.H : 0;
+  const int L = row_ok ? p.row_len[(int64_t)it.k * R + (int64_t)it.b * p.qlen + j] : 0;
+  const int row_end = min(L, it.t_end);  // tokens at or past it are invisible to this row
+  const float kv_scale = p.kv_scale ? *p.kv_scale : 1.0f;
+  const float sc = p.softmax_scale * kv_scale * kLog2e;
+
+  {
+    const uint16_t* src = p.q + ((int64_t)it.b * qrows + qr) * kDqk + d0;
+    const bool q_range = load_q<kFp8, kAtoms>(src, row_ok, h, r, tQ, sh.qs);
+    tc_fence_before();
+    fence_proxy_async_smem();
+    if (q_range) raise_status(p.status, DCP_STATUS_Q_RANGE);
+    mbar_arrive(&sh.bars[kBarQFull]);
+  }
+
+  const uint32_t peer = cta ^ 1;
+  const uint32_t xch_local = smem_u32(sh.xch);
+  const uint32_t xch_remote = mapa_shared(xch_local, peer);
+  const uint32_t xfull_remote = mapa_shared(smem_u32(&sh.bars[kBarXFull]), peer);
+  const uint32_t xfree_remote = mapa_shared(smem_u32(&sh.bars[kBarXFree]), peer);
+  const int32_t* pages = p.page_ids + ((int64_t)it.k * p.batch + it.b) * p.max_pages;
+  const int lg_sub = __ffs(p.subpage) - 1;
+  const int64_t pool_pages = p.pool_rows >> lg_sub;
+  const bool big_pages = p.subpage >= kTileN;
+
+  // Waits are made warp-uniform: the tcgen05.ld/st that follow are warp-collective.
+  auto wait_warp = [&](int bar, uint32_t parity, bool cluster) -> bool {
+    return __all_sync(0xffffffffu,
+                      wait_phase(&sh.bars[bar], parity, sh.abort_flag, p.status, cluster));
+  };
+  // The two warps sharing rows (w and w^4) combine per-row values through smem,
+  // synchronised by an mbarrier per (lane quarter, parity) with bounded waits.
+  auto pair_sync = [&](int i) -> bool {
+    uint64_t* bar = &sh.bars[kBarComb + qw * 2 + (i & 1)];
+    mbar_arrive(bar);
+    return __all_sync(0xffffffffu, wait_phase(bar, (i >> 1) & 1, sh.abort_flag, p.status, false));
+  };
+
+  const int n = it.n_tiles;
+  float M = -INFINITY;  // running reference (log2 units), same in both CTAs
+  float l_half = 0.f;   // sum of this half's weights
+  bool ok = true;
+  // own factors of the tile finished in the back half live in smem (registers are
+  // capped at 128 per thread with 14 warps): [half][group of 4][row] float4
+  float4* eprev = reinterpret_cast<float4*>(sh.eprev) + h * 8 * kRows + r;
+  float m_prev = -INFINITY;
+  int32_t pg_next = (big_pages && n > 0) ? __ldg(pages + (it.t_start >> lg_sub)) : 0;
+  for (int i = 0; i <= n; ++i) {
+    // ---------------- front: scores of tile i -> own factors -> peer
+    float e_cur[32];
+    float m_cur = -INFINITY;
+    if (i < n) {
+      const int tok0 = it.t_start + i * kTileN;
+      const int32_t pg_tile = pg_next;
+      if (!wait_warp(kBarSFullA, i & 1, false) || !wait_warp(kBarSFullB, i & 1, false)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int half16 = 0; half16 < 2; ++half16) {
+        uint32_t sa[16], sb[16];
+        tmem_ld16(tSa + 16 * half16, sa);
+        tmem_ld16(tSb + 16 * half16, sb);
+        tmem_wait_ld16(sa);
+        tmem_wait_ld16(sb);
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          e_cur[16 * half16 + c] = __uint_as_float(sa[c]) + __uint_as_float(sb[c]);
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.bars[kBarSFree]);
+      if (big_pages && i + 1 < n) pg_next = __ldg(pages + ((tok0 + kTileN) >> lg_sub));
+      // visible tokens of this row in this half: [tok0 + 32h, row_end), pages valid
+      const int cnt = max(0, min(32, row_end - tok0 - 32 * h));
+      const bool page_ok = !big_pages || (pg_tile >= 0 && pg_tile < pool_pages);
+      // e_cur := 2^(x*sc - m*sc + 14) with x the raw partial score (sc > 0)
+      if (cnt == 32 && big_pages && page_ok) {
+        // every token visible (all but a row's last tile): no masking
+        float mx = e_cur[0];
+#pragma unroll
+        for (int c = 1; c < 32; ++c) mx = fmaxf(mx, e_cur[c]);
+        m_cur = mx * sc;
+        const float bias = kFactorLog2 - m_cur;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) e_cur[c] = fast_exp2(fmaf(e_cur[c], sc, bias));
+      } else {
+        uint32_t vis = cnt >= 32 ? 0xFFFFFFFFu : ((1u << cnt) - 1u);
+        if (!page_ok) vis = 0;
+        if (!big_pages && vis) {
+          const int first = (tok0 + 32 * h) >> lg_sub;
+          const int last = (tok0 + 32 * h + cnt - 1) >> lg_sub;
+          for (int q = first; q <= last; ++q) {
+            const int32_t pg = pages[q];
+            if (pg < 0 || pg >= pool_pages) {
+              const int lo = max(0, (q << lg_sub) - (tok0 + 32 * h));
+              const int hi = min(32, ((q + 1) << lg_sub) - (tok0 + 32 * h));
+              const uint32_t m = (hi - lo >= 32) ? 0xFFFFFFFFu : (((1u << (hi - lo)) - 1u) << lo);
+              vis &= ~m;
+            }
+          }
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if ((vis >> c) & 1u) mx = fmaxf(mx, e_cur[c]);
+        m_cur = mx * sc;  // -inf if nothing is visible
+        const float bias = kFactorLog2 - m_cur;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          e_cur[c] = ((vis >> c) & 1u) ? fast_exp2(fmaf(e_cur[c], sc, bias)) : 0.f;
+      }
+      // send factors (f16 * 2^14) and m to the peer's slot i&1, free since tile i-2
+      const int slot = i & 1;
+      if (i >= 2 && !wait_warp(kBarXFree + slot, ((i >> 1) - 1) & 1, true)) {
+        ok = false;
+        break;
+      }
+      // st.async: each store completes its bytes on the peer's xfull[slot], which the
+      // peer armed with the slot size; no release fence is needed
+      const uint32_t dst = xch_remote + slot * kXchSlotBytes;
+      const uint32_t rbar = xfull_remote + 8 * slot;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          __half2 hh = __floats2half2_rn(e_cur[8 * g + 2 * e], e_cur[8 * g + 2 * e + 1]);
+          w4[e] = *reinterpret_cast<uint32_t*>(&hh);
+        }
+        st_async_v4(dst + (uint32_t)(((h * 4 + g) * kRows + r) * 16), w4[0], w4[1], w4[2],
+                    w4[3], rbar);
+      }
+      st_async_b32(dst + kXchEBytes + (uint32_t)((h * kRows + r) * 4), __float_as_uint(m_cur),
+                   rbar);
+    }
+    // ---------------- back: finish tile t = i-1 with the peer's factors
+    if (i >= 1) {
+      const int t = i - 1;
+      const int slot = t & 1;
+      // one thread arms this use of the slot with its size (the bytes may already be in)
+      if (tid == 0) mbar_arrive_expect_tx(&sh.bars[kBarXFull + slot], kXchSlotBytes);
+      if (!wait_warp(kBarXFull + slot, (t >> 1) & 1, true)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* src = sh.xch + slot * kXchSlotBytes;
+      const float m_peer = *reinterpret_cast<const float*>(src + kXchEBytes + (h * kRows + r) * 4);
+      uint4 pe[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+        pe[g] = *reinterpret_cast<const uint4*>(src + ((h * 4 + g) * kRows + r) * 16);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(xfree_remote + 8 * slot);  // done with the peer's slot
+      // tile bound of the row (max over both halves of m_own + m_peer)
+      const float ub_h =
+          (m_prev == -INFINITY || m_peer == -INFINITY) ? -INFINITY : m_prev + m_peer;
+      float* comb = sh.comb + (t & 1) * 2 * kRows;
+      comb[h * kRows + r] = ub_h;
+      if (!pair_sync(t)) {
+        ok = false;
+        break;
+      }
+      const float ub = fmaxf(ub_h, comb[(h ^ 1) * kRows + r]);
+      const bool need = ub != -INFINITY && (M == -INFINITY || ub > M + kRescaleThreshold);
+      float alpha = 1.f;
+      if (need) {
+        alpha = M == -INFINITY ? 0.f : fast_exp2(M - ub);
+        l_half *= alpha;
+        M = ub;
+      }
+      // PV(t-1) done: P buffer is free and O is stable
+      if (t >= 1 && !wait_warp(kBarODone, (t - 1) & 1, false)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (t >= 1 && __any_sync(0xffffffffu, need)) rescale_o(tO, need ? alpha : 1.f);
+      // p = E_own * E_peer * 2^(m_own + m_peer - M); both factors carry 2^14. 8 tokens at a time
+      const float f = ub_h == -INFINITY ? 0.f : fast_exp2(ub_h - M - 2.0f * kFactorLog2);
+      float lsum = 0.f;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const float4 own0 = eprev[(2 * g) * kRows];
+        const float4 own1 = eprev[(2 * g + 1) * kRows];
+        const float ow[8] = {own0.x, own0.y, own0.z, own0.w, own1.x, own1.y, own1.z, own1.w};
+        const uint32_t pw[4] = {pe[g].x, pe[g].y, pe[g].z, pe[g].w};
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 ep = __half22float2(*reinterpret_cast<const __half2*>(&pw[e]));
+          const float p0 = ow[2 * e] * ep.x * f;
+          const float p1 = ow[2 * e + 1] * ep.y * f;
+          // l sums the fp32 weights; the P.V contraction uses P rounded to 16 bits
+          lsum += p0 + p1;
+          if (kFp8) {
+            __half2 hh = __floats2half2_rn(p0, p1);
+            pk[e] = *reinterpret_cast<uint32_t*>(&hh);
+          } else {
+            __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+            pk[e] = *reinterpret_cast<uint32_t*>(&hh);
+          }
+        }
+        tmem_st4(tP + 4 * g, pk);
+      }
+      l_half += lsum;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&sh.bars[kBarPFull]);
+    }
+    if (i < n) {
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        eprev[g * kRows] =
+            make_float4(e_cur[4 * g], e_cur[4 * g + 1], e_cur[4 * g + 2], e_cur[4 * g + 3]);
+    }
+    m_prev = m_cur;
+  }
+
+  // epilogue: both halves' l, then this warp's 128 O columns of its rows
+  const bool have_o =
+      __all_sync(0xffffffffu, ok) && n > 0 && wait_warp(kBarODone, (n - 1) & 1, false);
+  tc_fence_after();
+  float* comb = sh.comb + (n & 1) * 2 * kRows;
+  comb[h * kRows + r] = l_half;
+  const bool paired = pair_sync(n);
+  const float l_run = l_half + comb[(h ^ 1) * kRows + r];
+  const int64_t rh = (int64_t)it.b * qrows + qr;
+  const int64_t base = ((int64_t)it.k * p.num_splits + it.s) * ((int64_t)R * p.H) + rh;
+  const float inv = (paired && l_run > 0.f) ? kv_scale / l_run : 0.f;
+  store_o(tO, have_o, row_ok, inv, p.part_o + base * kDv + 256 * cta + 128 * h);
   if (row_ok && cta == 0 && h == 0) {
     p.part_m[base] = l_run > 0.f ? M : -INFINITY;
     p.part_l[base] = l_run;
@@ -670,19 +824,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sh.bars[kBarKvFull + i], 128);
-      mbar_init(&sh.bars[kBarKvEmpty + i], 1);
+      mbar_init(&sh.bars[kBarKvEmpty + i], 2);
     }
-    mbar_init(&sh.bars[kBarSFull], 1);
+    mbar_init(&sh.bars[kBarSFullA], 1);
+    mbar_init(&sh.bars[kBarSFullB], 1);
     mbar_init(&sh.bars[kBarSFree], kSoftWarps * 32);
     mbar_init(&sh.bars[kBarPFull], kSoftWarps * 32);
     mbar_init(&sh.bars[kBarODone], 1);
     mbar_init(&sh.bars[kBarQFull], kSoftWarps * 32);
     for (int i = 0; i < kXchSlots; ++i) {
-      mbar_init(&sh.bars[kBarXFull + i], kSoftWarps);  // one elected arrival per peer warp
+      mbar_init(&sh.bars[kBarXFull + i], 1);  // armed by one local thread + the slot's bytes
       mbar_init(&sh.bars[kBarXFree + i], kSoftWarps);
     }
     for (int i = 0; i < 8; ++i) mbar_init(&sh.bars[kBarComb + i], 64);
-    mbar_init(&sh.bars[kBarDrain], 1);
+    mbar_init(&sh.bars[kBarDrainA], 1);
+    mbar_init(&sh.bars[kBarDrainB], 1);
     *sh.abort_flag = 0;
     fence_mbarrier_init_cluster();
     const int64_t sb = ((int64_t)it.k * p.batch + it.b) * p.num_splits + it.s;
@@ -690,7 +846,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (cta == 0 && it.t == 0 && (beg < 0 || end < beg || end > p.max_pages))
       raise_status(p.status, DCP_STATUS_BAD_SPLIT);
   }
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarpA) {
     tmem_alloc(sh.tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -703,17 +859,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp < kSoftWarps) {
     if (cta == 0) run_softmax<kFp8, 4>(p, sh, it, tbase, tid);
     else run_softmax<kFp8, 5>(p, sh, it, tbase, tid);
-  } else if (warp < kMmaWarp) {
+  } else if (warp < kMmaWarpA) {
     if (cta == 0) Producer<kFp8, 4>(p, sh, it, tid - kProdWarp0 * 32).run();
     else Producer<kFp8, 5>(p, sh, it, tid - kProdWarp0 * 32).run();
-  } else if (tid == kMmaWarp * 32) {
-    if (cta == 0) run_mma<kFp8, 4>(p, sh, it, tbase);
-    else run_mma<kFp8, 5>(p, sh, it, tbase);
+  } else if (tid == kMmaWarpA * 32) {
+    if (cta == 0) run_mma_a<kFp8, 4>(p, sh, it, tbase);
+    else run_mma_a<kFp8, 5>(p, sh, it, tbase);
+  } else if (tid == kMmaWarpB * 32) {
+    if (cta == 0) run_mma_b<kFp8, 4>(p, sh, it, tbase);
+    else run_mma_b<kFp8, 5>(p, sh, it, tbase);
   }
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // the peer no longer touches this CTA's shared memory
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarpA) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
