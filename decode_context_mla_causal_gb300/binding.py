@@ -84,6 +84,7 @@ def load() -> ctypes.CDLL:
         "dcp_mla_metadata": (I, [D, P, P, I, I, P, P, P, P, P, P]),
         "dcp_mla_partial": (I, [D, P, P, I, P, ctypes.c_float, I, I, P, P, P, P, P, P, P, P, P]),
         "dcp_lse_merge": (I, [D, I, P, P, P, P, P, P, P, P]),
+        "dcp_mla_verify_noalloc": (I, [D, P, P, P, P, I, P, ctypes.c_float, P, P, P, P]),
         "dcp_last_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -200,3 +201,21 @@ def dcp_lse_merge(dims, num_ranks, part_o, part_m, part_l, out, lse, rank_lse=No
         _ptr(lse, f32, R * H, "lse"),
         _ptr(rank_lse, f32, num_ranks * R * H, "rank_lse", allow_none=True),
         _ptr(status, torch.int32, 1, "status"), _stream(stream)))
+
+
+def dcp_mla_verify_noalloc(dims, seq_lens, block_table, q, kv, kv_dtype, kv_scale,
+                           softmax_scale, out, lse, status, stream=None):
+    """The whole verify step over the library's fixed device scratch (no allocation)."""
+    lib = load()
+    B, R, H = dims.batch, dims.rows, dims.num_heads
+    i32, f32 = torch.int32, torch.float32
+    kv_elem = torch.uint8 if kv_dtype == KV_FP8_E4M3 else torch.bfloat16
+    pool = dims.num_blocks * dims.block_size * QK_DIM
+    _check(lib.dcp_mla_verify_noalloc(
+        ctypes.byref(dims), _ptr(seq_lens, i32, B, "seq_lens"),
+        _ptr(block_table, i32, B * dims.max_blocks_per_seq, "block_table"),
+        _ptr(q, torch.bfloat16, R * H * QK_DIM, "q"),
+        _ptr(kv, kv_elem, dims.dcp * pool, "kv"), int(kv_dtype),
+        _ptr(kv_scale, f32, 1, "kv_scale", allow_none=True), float(softmax_scale),
+        _ptr(out, torch.bfloat16, R * H * V_DIM, "out"), _ptr(lse, f32, R * H, "lse"),
+        _ptr(status, i32, 1, "status"), _stream(stream)))

@@ -200,6 +200,29 @@ dcp_status dcp_lse_merge(const dcp_mla_dims* dims, int32_t num_ranks, const floa
                          const float* part_m, const float* part_l, void* out, float* lse,
                          float* rank_lse, uint32_t* status, dcp_stream_t stream);
 
+/*
+ * The whole verify step (metadata, partial attention and merge over all dcp
+ * ranks, exactly as the three calls above with dims->num_splits) for callers
+ * that cannot allocate device memory: the pages have no counterpart of this
+ * call; it exists for code that must not call cudaMalloc (inside allocator
+ * callbacks, or under a runtime that owns the device heap).
+ *
+ *   seq_lens, block_table, q, kv, kv_scale, softmax_scale: as above
+ *   out  device bf16 [R][H][512], lse device float [R][H]: as dcp_lse_merge
+ *   status device uint32 [1]: in/out, as above
+ * Intermediates live in a fixed 32 MiB device array inside the library (held on
+ * every GPU that loads it until exit); dims needing more return
+ * DCP_ERR_UNSUPPORTED before any launch. The call allocates nothing. The first
+ * call on a device looks up the array's device address (make that first call
+ * before any stream capture on that device). Every call shares the array and it
+ * keeps the last call's contents: calls that overlap on the GPU race.
+ */
+dcp_status dcp_mla_verify_noalloc(const dcp_mla_dims* dims, const int32_t* seq_lens,
+                                  const int32_t* block_table, const void* q, const void* kv,
+                                  dcp_kv_dtype kv_dtype, const float* kv_scale,
+                                  float softmax_scale, void* out, float* lse, uint32_t* status,
+                                  dcp_stream_t stream);
+
 /* Message for the last non-OK return on this thread ("" if none). */
 const char* dcp_last_error(void);
 
