@@ -25,24 +25,21 @@ def choose_num_splits(batch: int, qlen: int, num_heads: int, num_ranks: int,
     """Static split count for the partial kernel.
 
     Each work item (rank, sequence, split, 128-row tile) runs on a cluster of two
-    CTAs, one CTA per SM, so ``sms // 2`` items run at once. Pick the split count
-    whose item count fills the last wave best (within 3 % of the best, the
-    smallest such count), keeping at least eight subpages of work per split at
-    the static bound. Uses only static sizes, so the choice is graph-safe.
+    CTAs, one CTA per SM, so ``sms // 2`` items run at once. The cost model is
+    waves * (64-token tiles per split + 2 tiles of per-item overhead), evaluated
+    at the static bound; the cheapest split count wins (ties: fewer splits).
+    Uses only static sizes, so the choice is graph-safe.
     """
-    P = B.dcp_mla_subpage_size(block_size)
-    pages = max(1, math.ceil(max_local_len / P))
-    tiles = math.ceil(qlen * num_heads / 128)
-    base = max(1, batch * num_ranks * tiles)
+    tiles = max(1, math.ceil(max_local_len / 64))
+    row_tiles = math.ceil(qlen * num_heads / 128)
+    base = max(1, batch * num_ranks * row_tiles)
     slots = max(1, sms // 2)
-    max_ns = max(1, min(64, pages // 8))
-    best = []
-    for ns in range(1, max_ns + 1):
-        items = base * ns
-        eff = items / (math.ceil(items / slots) * slots)
-        best.append((eff, ns))
-    top = max(e for e, _ in best)
-    return int(min(ns for e, ns in best if e >= 0.97 * top))
+    best = None
+    for ns in range(1, min(64, tiles) + 1):
+        cost = math.ceil(base * ns / slots) * (tiles / ns + 2.0)
+        if best is None or cost < best[0] - 1e-9:
+            best = (cost, ns)
+    return int(best[1])
 
 
 def make_dims(*, batch, qlen, num_heads, dcp, interleave, block_size, max_blocks_per_seq,
