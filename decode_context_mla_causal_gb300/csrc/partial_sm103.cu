@@ -722,12 +722,6 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
       }
       const uint8_t* src = sh.xch + slot * kXchSlotBytes;
       const float m_peer = *reinterpret_cast<const float*>(src + kXchEBytes + (h * kRows + r) * 4);
-      uint4 pe[4];
-#pragma unroll
-      for (int g = 0; g < 4; ++g)
-        pe[g] = *reinterpret_cast<const uint4*>(src + ((h * 4 + g) * kRows + r) * 16);
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(xfree_remote + 8 * slot);  // done with the peer's slot
       // tile bound of the row (max over both halves of m_own + m_peer)
       const float ub_h =
           (m_prev == -INFINITY || m_peer == -INFINITY) ? -INFINITY : m_prev + m_peer;
@@ -752,21 +746,24 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
       }
       tc_fence_after();
       if (t >= 1 && __any_sync(0xffffffffu, need)) rescale_o(tO, need ? alpha : 1.f);
-      // p = E_own * E_peer * 2^(m_own + m_peer - M); both factors carry 2^14. 8 tokens at a time
+      // p = E_own * E_peer * 2^(m_own + m_peer - M); both factors carry 2^14. 8 tokens per
+      // (rolled) step, read from the peer's slot and this thread's own-factor buffer
       const float f = ub_h == -INFINITY ? 0.f : fast_exp2(ub_h - M - 2.0f * kFactorLog2);
       float lsum = 0.f;
-#pragma unroll
+      const uint4* pe_src = reinterpret_cast<const uint4*>(src) + h * 4 * kRows + r;
+#pragma unroll 1
       for (int g = 0; g < 4; ++g) {
+        const uint4 pe = pe_src[g * kRows];
         const float4 own0 = eprev[(2 * g) * kRows];
         const float4 own1 = eprev[(2 * g + 1) * kRows];
         const float ow[8] = {own0.x, own0.y, own0.z, own0.w, own1.x, own1.y, own1.z, own1.w};
-        const uint32_t pw[4] = {pe[g].x, pe[g].y, pe[g].z, pe[g].w};
+        const uint32_t pw[4] = {pe.x, pe.y, pe.z, pe.w};
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 ep = __half22float2(*reinterpret_cast<const __half2*>(&pw[e]));
-          const float p0 = ow[2 * e] * ep.x * f;
-          const float p1 = ow[2 * e + 1] * ep.y * f;
+          const float p0 = ow[2 * e] * f * ep.x;
+          const float p1 = ow[2 * e + 1] * f * ep.y;
           // l sums the fp32 weights; the P.V contraction uses P rounded to 16 bits
           lsum += p0 + p1;
           if (kFp8) {
@@ -779,6 +776,8 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
         }
         tmem_st4(tP + 4 * g, pk);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(xfree_remote + 8 * slot);  // done with the peer's slot
       l_half += lsum;
       tmem_wait_st();
       tc_fence_before();
