@@ -14,47 +14,52 @@
 //   * Both CTAs need the full scores. Instead of computing them twice, the 576
 //     q/k dims are split too: CTA0 computes the partial score x0 over dims
 //     [0, 256), CTA1 x1 over dims [256, 576) (log2 units). Shared memory across
-//     the pair is slow (about 25 GB/s per SM each way), so a CTA does not send x
-//     itself: for each (row, 32-token half) it sends its own maximum m_c and the
-//     factors E_c = 2^(x_c - m_c) in f16 (scaled by 2^14, so values down to
-//     2^-28 keep 11 bits). The receiver forms
+//     the pair is slow (about 18 bytes per cycle per SM each way, measured), so a
+//     CTA does not send x itself: for each (row, 32-token half) it sends its own
+//     maximum m_c and the factors E_c = 2^(x_c - m_c) in f16 (scaled by 2^14, so
+//     values down to 2^-28 keep 11 bits). The receiver forms
 //         p = E_own * E_peer * 2^(m_own + m_peer - M),
-//     where M is the running reference, updated only when the tile bound
-//     m_own + m_peer exceeds it by more than 8 (then O and l are rescaled). The
-//     bound is an upper bound of the true maximum, so p <= 2^8. Relative error
-//     of p and l from the f16 factor: at most 2^-12. Both CTAs agree on M (sums of
-//     the same two floats), so their l and P agree to that error; each CTA
-//     normalises its own half of O by its own l.
+//     where M is the running reference of the row, raised only when the tile
+//     bound max_half(m_own + m_peer) exceeds it by more than 8 (then O and l are
+//     rescaled). The bound is an upper bound of the true maximum, so p <= 2^8.
+//     Relative error of p and l from the f16 factor: at most 2^-11. Both CTAs
+//     agree on M (sums of the same two floats), so their l and P agree to that
+//     error; each CTA normalises its own half of O by its own l.
 //   * CTA c stages dims [256c, 256c + 256 + 64c) of every token: its q.k slice,
 //     which also holds its value slice.
-//   * A tcgen05.mma of M=128 costs about 190 cycles of issue latency per thread
-//     whatever its N (measured), so N=64 score MMAs only reach full rate when
-//     several warps issue independent chains. The q.k contraction is therefore
-//     split into two chains with their own accumulators, issued by two warps:
-//     chain A (dims atoms 0-1, q operand in TMEM) and chain B (atoms 2.., q
-//     operand in shared memory); the softmax adds the two partial scores.
+//   * One thread issuing tcgen05.mma alone gets about one instruction per 280
+//     cycles whatever N is; two or three issuing warps each get about one per
+//     130-230 cycles (measured). So the q.k contraction is split into two chains
+//     of equal length with their own accumulators, and P.V has its own issuer:
+//     three issuing warps. The softmax adds the two partial scores.
 //   * The factor exchange runs one tile behind: iteration i loads the scores of
 //     tile i and sends its factors, then finishes tile i-1 with the factors the
 //     peer sent an iteration earlier, so the exchange latency overlaps work.
+//     P.V has its own issuing warp and starts as soon as P is written, so the
+//     next P write (one iteration later) rarely waits for it.
 //
-// Per CTA (448 threads):
+// Per CTA (480 threads):
 //   warps 0-7   softmax: warp w owns rows 32*(w%4) .. +31 (TMEM lane quarter)
 //               and token half w/4 of every 64-token tile; Q (TMEM + smem),
 //               factor exchange (double-buffered slots), lazy online softmax,
 //               P (16-bit) into TMEM, epilogue for O columns [128*(w/4), +128).
+//               The partner warp's half maximum comes through shared memory
+//               behind a per-tile barrier; a thread keeps its own factors of
+//               the previous tile in shared memory.
 //   warps 8-11  KV producers: 16-byte loads of the paged cache rows (subpage ids
 //               from the metadata, bounds-checked, two tiles in flight), FP8
 //               E4M3 -> f16 conversion, stores into 128-byte-swizzled K-major
 //               tiles of a 3-stage ring.
-//   warp 12     TMEM allocation; one thread issues chain A of S(i)
-//               (Q[tmem] . K_tile^T, M=128 N=64) and O += P[tmem] . V_tile
-//               (M=128, N=256, V read MN-major from the same swizzled tile).
-//   warp 13     one thread issues chain B of S(i) (Q[smem] . K_tile^T).
+//   warp 12     TMEM allocation; one thread issues score chain A (k-steps
+//               [0, K/2): q atoms 0-2 from TMEM, the rest from shared memory).
+//   warp 13     one thread issues score chain B (k-steps [K/2, K), q from smem).
+//   warp 14     one thread issues O += P[tmem] . V_tile (M=128, N=256, V read
+//               MN-major from the same swizzled tile as K).
 // TMEM columns: O [0,256), S_a [256,320), S_b [320,384), P [384,416),
-// Q chain A [416,480). The FP8-cache path computes in f16 (E4M3 -> f16 is exact;
-// q is BF16 -> f16, exact in f16's normal range; |q| > 65504 sets
-// DCP_STATUS_Q_RANGE); the BF16-cache path computes in bf16. Accumulation is
-// fp32 throughout.
+// Q atoms 0-2 [416,512). The FP8-cache path computes in f16
+// (E4M3 -> f16 is exact; q is BF16 -> f16, exact in f16's normal range;
+// |q| > 65504 sets DCP_STATUS_Q_RANGE); the BF16-cache path computes in bf16.
+// Accumulation is fp32 throughout.
 //
 // Every wait is bounded (DCP_STATUS_TIMEOUT and an orderly exit: all roles stop,
 // in-flight MMAs are drained, TMEM is freed). Waiting threads sleep in
@@ -78,20 +83,22 @@ constexpr int kMaxAtoms = 5;   // 64-dim swizzle atoms staged per CTA (CTA1: 320
 constexpr int kAtomBytes = kTileN * 128;
 constexpr int kStageBytes = kMaxAtoms * kAtomBytes;
 constexpr int kQAtomBytes = kRows * 128;       // one 64-dim atom of Q (128 rows)
-constexpr int kChainAAtoms = 2;                // q.k atoms 0..1 form chain A, the rest chain B
 constexpr int kQTmemAtoms = 3;                 // q atoms 0..2 live in TMEM, 3.. in smem
 constexpr int kQSmemBytes = (kMaxAtoms - kQTmemAtoms) * kQAtomBytes;
-constexpr int kEPrevBytes = 2 * kTileN / 2 * kRows * 4;  // own fp32 factors [half][32][row]
 // factor exchange slot: E as f16 [half 2][group 4][row 128][8 values], m as f32 [half][row]
 constexpr int kXchEBytes = 2 * 4 * kRows * 16;
 constexpr int kXchSlotBytes = kXchEBytes + 2 * kRows * 4;
 constexpr int kXchSlots = 2;
-constexpr int kCombBytes = 2 * 2 * kRows * 4;  // [parity][half][row] f32 for the half combine
+constexpr int kMOwnBufs = 3;                            // own half maxima, by tile mod 3
+constexpr int kMOwnBytes = kMOwnBufs * 2 * kRows * 4;   // [tile%3][half][row] f32
+constexpr int kLCombBytes = 2 * kRows * 4;              // [half][row] f32, epilogue
+constexpr int kEPrevBytes = 2 * kTileN / 2 * kRows * 4;  // own fp32 factors [half][32][row]
 constexpr int kSoftWarps = 8;
 constexpr int kProdWarp0 = 8;
 constexpr int kMmaWarpA = 12;
 constexpr int kMmaWarpB = 13;
-constexpr int kThreads = 14 * 32;
+constexpr int kMmaWarpP = 14;
+constexpr int kThreads = 15 * 32;
 constexpr uint32_t kColO = 0, kColSa = 256, kColSb = 320, kColP = 384, kColQ = 416;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // P may grow to 2^8 before O is rescaled
@@ -103,24 +110,26 @@ constexpr float kLog2e = 1.4426950408889634f;
 // barrier slots
 enum {
   kBarKvFull = 0,
-  kBarKvEmpty = kBarKvFull + kStages,  // count 2: PV (chain A thread) and chain B
-  kBarSFullA = kBarKvEmpty + kStages,
-  kBarSFullB,
-  kBarSFree,
-  kBarPFull,
-  kBarODone,
-  kBarQFull,
-  kBarXFull,                          // [2] the peer's factors are in my slot
-  kBarXFree = kBarXFull + kXchSlots,  // [2] the peer consumed what I wrote into its slot
-  kBarComb = kBarXFree + kXchSlots,   // [4 lane quarters][2 parities] half-combine, count 64
-  kBarDrainA = kBarComb + 8,
+  kBarKvEmpty = kBarKvFull + kStages,  // count 3: chain A, chain B, P.V
+  kBarSFull = kBarKvEmpty + kStages,   // count 2: chain A, chain B
+  kBarSFree,                           // count 8: softmax warps read S
+  kBarPFull,                           // count 8: P written
+  kBarODone,                           // P.V completed
+  kBarQFull,                           // count 8
+  kBarXFull,                           // [2] the peer's factors are in my slot
+  kBarXFree = kBarXFull + kXchSlots,   // [2] count 8: the peer consumed what I wrote
+  kBarMOwn = kBarXFree + kXchSlots,    // [3] count 8: own half maxima of a tile written
+  kBarLComb = kBarMOwn + kMOwnBufs,    // count 8: epilogue l halves written
+  kBarDrainA,
   kBarDrainB,
+  kBarDrainP,
   kNumBars
 };
 
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kQSmemBytes +
-                              kXchSlots * kXchSlotBytes + kCombBytes + kEPrevBytes +
-                              kNumBars * 8 + 16;
+                              kXchSlots * kXchSlotBytes + kMOwnBytes + kLCombBytes +
+                              kEPrevBytes + kNumBars * 8 + 16;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct Params {
   const uint16_t* q;
@@ -141,10 +150,11 @@ struct Params {
 
 struct Shared {
   uint8_t* stages;
-  uint8_t* qs;   // Q atoms kQTmemAtoms.. (shared-memory operand of chain B)
-  uint8_t* xch;  // kXchSlots slots
-  float* comb;
-  float* eprev;  // own factors of the tile awaiting the peer's
+  uint8_t* qs;    // Q atoms kQTmemAtoms.. (shared-memory operand)
+  uint8_t* xch;   // kXchSlots slots
+  float* mown;    // own half maxima per tile
+  float* lcomb;   // epilogue l halves
+  float* eprev;   // own factors of the tile awaiting the peer's
   uint64_t* bars;
   uint32_t* tmem_slot;
   int* abort_flag;
@@ -157,8 +167,9 @@ __device__ __forceinline__ Shared carve(unsigned char* raw) {
   s.stages = base;
   s.qs = base + kStages * kStageBytes;
   s.xch = s.qs + kQSmemBytes;
-  s.comb = reinterpret_cast<float*>(s.xch + kXchSlots * kXchSlotBytes);
-  s.eprev = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s.comb) + kCombBytes);
+  s.mown = reinterpret_cast<float*>(s.xch + kXchSlots * kXchSlotBytes);
+  s.lcomb = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s.mown) + kMOwnBytes);
+  s.eprev = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s.lcomb) + kLCombBytes);
   s.bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.eprev) + kEPrevBytes);
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + kNumBars);
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
@@ -384,63 +395,21 @@ struct Producer {
 };
 
 // ----------------------------------------------------------------- MMA issuers
-// Chain A of every score tile plus every P.V; PV(j) is issued two tiles late
-// (after the score chain of tile j+2), because P(j) is finished one softmax
-// iteration after S(j) is read.
-template <bool kFp8, int kAtoms>
-__device__ __forceinline__ void run_mma_a(const Params& p, const Shared& sh, const Item& it,
-                                          uint32_t tbase) {
-  const uint32_t idq = idesc_f16(kRows, kTileN, !kFp8, false);
-  const uint32_t idp = idesc_f16(kRows, 256, !kFp8, true);
-  const uint32_t stage0 = smem_u32(sh.stages);
-  bool ok = wait_phase(&sh.bars[kBarQFull], 0, sh.abort_flag, p.status, false);
-  tc_fence_after();
-  auto issue_pv = [&](int j) -> bool {
-    if (!wait_phase(&sh.bars[kBarPFull], j & 1, sh.abort_flag, p.status, false)) return false;
-    tc_fence_after();
-    const uint32_t sa = stage0 + (j % kStages) * kStageBytes;
-#pragma unroll
-    for (int kk = 0; kk < kTileN / 16; ++kk) {
-      const uint64_t d = smem_desc_sw128(sa + kk * 2048, kAtomBytes, 1024);
-      mma_f16_ts(tbase + kColO, tbase + kColP + 8 * kk, d, idp, (j > 0 || kk > 0) ? 1u : 0u);
-    }
-    tc_commit(&sh.bars[kBarODone]);
-    tc_commit(&sh.bars[kBarKvEmpty + (j % kStages)]);
-    return true;
-  };
-  const int n = it.n_tiles;
-  for (int i = 0; ok && i < n + 2; ++i) {
-    if (i < n) {
-      const int st = i % kStages;
-      if (!wait_phase(&sh.bars[kBarKvFull + st], (i / kStages) & 1, sh.abort_flag, p.status,
-                      false))
-        break;
-      if (i >= 1 && !wait_phase(&sh.bars[kBarSFree], (i - 1) & 1, sh.abort_flag, p.status, false))
-        break;
-      tc_fence_after();
-      const uint32_t sa = stage0 + st * kStageBytes;
-#pragma unroll
-      for (int kk = 0; kk < 4 * kChainAAtoms; ++kk) {
-        const uint64_t d = smem_desc_sw128(sa + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024);
-        mma_f16_ts(tbase + kColSa, tbase + kColQ + 8 * kk, d, idq, kk > 0 ? 1u : 0u);
-      }
-      tc_commit(&sh.bars[kBarSFullA]);
-    }
-    if (i >= 2 && !issue_pv(i - 2)) ok = false;
-  }
-  // drain: every MMA issued above has completed before TMEM can be released
-  tc_commit(&sh.bars[kBarDrainA]);
-  int never = 0;
-  wait_phase(&sh.bars[kBarDrainA], 0, &never, p.status, false);
-}
+// A thread issuing tcgen05.mma back to back gets about one instruction per
+// 55-130 cycles (N = 64..256), but any branch or non-trivial arithmetic between
+// two of them was measured to double that. So each chain is a fully unrolled
+// straight line whose descriptors are per-tile bases plus constants (the
+// address field of a descriptor is the byte address / 16 in its low bits).
 
-// Chain B of every score tile (q operand from shared memory).
-template <bool kFp8, int kAtoms>
-__device__ __forceinline__ void run_mma_b(const Params& p, const Shared& sh, const Item& it,
-                                          uint32_t tbase) {
-  const uint32_t idq = idesc_f16(kRows, kTileN, !kFp8, false);
+// Score chain over k-steps [KK0, KK1) of this CTA's 4*kAtoms (16 dims each) into
+// the accumulator at column kAcc. q atoms 0..kQTmemAtoms-1 come from TMEM, the
+// rest from shared memory.
+template <bool kFp8, int kAtoms, int KK0, int KK1, uint32_t kAcc, int kDrainBar>
+__device__ __forceinline__ void run_score_chain(const Params& p, const Shared& sh, const Item& it,
+                                                uint32_t tbase) {
+  constexpr uint32_t idq = idesc_f16(kRows, kTileN, !kFp8, false);
   const uint32_t stage0 = smem_u32(sh.stages);
-  const uint32_t q0 = smem_u32(sh.qs);
+  const uint64_t qdesc0 = smem_desc_sw128(smem_u32(sh.qs), 16, 1024);
   if (wait_phase(&sh.bars[kBarQFull], 0, sh.abort_flag, p.status, false)) {
     tc_fence_after();
     for (int i = 0; i < it.n_tiles; ++i) {
@@ -451,26 +420,51 @@ __device__ __forceinline__ void run_mma_b(const Params& p, const Shared& sh, con
       if (i >= 1 && !wait_phase(&sh.bars[kBarSFree], (i - 1) & 1, sh.abort_flag, p.status, false))
         break;
       tc_fence_after();
-      const uint32_t sa = stage0 + st * kStageBytes;
+      const uint64_t bdesc0 = smem_desc_sw128(stage0 + st * kStageBytes, 16, 1024);
 #pragma unroll
-      for (int kk = 4 * kChainAAtoms; kk < 4 * kAtoms; ++kk) {
-        const uint64_t b = smem_desc_sw128(sa + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024);
-        const uint32_t acc = kk > 4 * kChainAAtoms ? 1u : 0u;
+      for (int kk = KK0; kk < KK1; ++kk) {
+        const uint64_t b = bdesc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
+        const uint32_t acc = kk > KK0 ? 1u : 0u;
         if ((kk >> 2) < kQTmemAtoms) {
-          mma_f16_ts(tbase + kColSb, tbase + kColQ + 8 * kk, b, idq, acc);
+          mma_f16_ts(tbase + kAcc, tbase + kColQ + 8 * kk, b, idq, acc);
         } else {
-          const uint64_t a = smem_desc_sw128(
-              q0 + ((kk >> 2) - kQTmemAtoms) * kQAtomBytes + (kk & 3) * 32, 16, 1024);
-          mma_f16_ss(tbase + kColSb, a, b, idq, acc);
+          const uint64_t a =
+              qdesc0 + (uint64_t)((((kk >> 2) - kQTmemAtoms) * kQAtomBytes + (kk & 3) * 32) >> 4);
+          mma_f16_ss(tbase + kAcc, a, b, idq, acc);
         }
       }
-      tc_commit(&sh.bars[kBarSFullB]);
+      tc_commit(&sh.bars[kBarSFull]);
       tc_commit(&sh.bars[kBarKvEmpty + st]);
     }
   }
-  tc_commit(&sh.bars[kBarDrainB]);
+  // drain: every MMA issued above has completed before TMEM can be released
+  tc_commit(&sh.bars[kDrainBar]);
   int never = 0;
-  wait_phase(&sh.bars[kBarDrainB], 0, &never, p.status, false);
+  wait_phase(&sh.bars[kDrainBar], 0, &never, p.status, false);
+}
+
+// O += P(j) . V(j) for every tile, as soon as the softmax has written P(j).
+template <bool kFp8>
+__device__ __forceinline__ void run_pv(const Params& p, const Shared& sh, const Item& it,
+                                       uint32_t tbase) {
+  constexpr uint32_t idp = idesc_f16(kRows, 256, !kFp8, true);
+  const uint32_t stage0 = smem_u32(sh.stages);
+  for (int j = 0; j < it.n_tiles; ++j) {
+    if (!wait_phase(&sh.bars[kBarPFull], j & 1, sh.abort_flag, p.status, false)) break;
+    tc_fence_after();
+    const uint64_t vdesc0 = smem_desc_sw128(stage0 + (j % kStages) * kStageBytes, kAtomBytes, 1024);
+    const uint32_t tp = tbase + kColP;
+    const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+    for (int kk = 0; kk < kTileN / 16; ++kk)
+      mma_f16_ts(tbase + kColO, tp + 8 * kk, vdesc0 + (uint64_t)((kk * 2048) >> 4), idp,
+                 kk > 0 ? 1u : acc0);
+    tc_commit(&sh.bars[kBarODone]);
+    tc_commit(&sh.bars[kBarKvEmpty + (j % kStages)]);
+  }
+  tc_commit(&sh.bars[kBarDrainP]);
+  int never = 0;
+  wait_phase(&sh.bars[kBarDrainP], 0, &never, p.status, false);
 }
 
 // ----------------------------------------------------------------- softmax
@@ -487,6 +481,7 @@ __device__ __noinline__ void rescale_o(uint32_t tO, float a) {
     for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
     tmem_st16(tO + 16 * c8, o);
   }
+  tmem_wait_st();
 }
 
 // Stores this warp's rows of the normalised partial output (128 columns).
@@ -513,14 +508,14 @@ __device__ __noinline__ void store_o(uint32_t tO, bool have_o, bool row_ok, floa
 }
 
 // Q slice of one row: atoms 0..kQTmemAtoms-1 -> TMEM, the rest -> smem (swizzled
-// K-major); half 0 loads atoms 0-1, half 1 the rest. Returns true if some |q|
-// exceeds the f16 range on the FP8 path.
+// K-major); half 0 loads the TMEM atoms, half 1 the rest. Returns true if some
+// |q| exceeds the f16 range on the FP8 path.
 template <bool kFp8, int kAtoms>
 __device__ __noinline__ bool load_q(const uint16_t* src, bool row_ok, int h, int r, uint32_t tQ,
                                     uint8_t* qs) {
   bool q_range = false;
-  const int a0 = h == 0 ? 0 : 2;
-  const int a1 = h == 0 ? 2 : kAtoms;
+  const int a0 = h == 0 ? 0 : kQTmemAtoms;
+  const int a1 = h == 0 ? kQTmemAtoms : kAtoms;
   for (int a = a0; a < a1; ++a) {
     uint32_t w[32];
 #pragma unroll
@@ -555,6 +550,24 @@ __device__ __noinline__ bool load_q(const uint16_t* src, bool row_ok, int h, int
   return q_range;
 }
 
+// Tokens of one (row, half) whose subpage id is invalid, when subpages are
+// shorter than a tile (one tile spans several subpages): clears their bits.
+__device__ __noinline__ uint32_t small_page_mask(uint32_t vis, const int32_t* pages, int first_tok,
+                                                 int cnt, int lg_sub, int64_t pool_pages) {
+  const int first = first_tok >> lg_sub;
+  const int last = (first_tok + cnt - 1) >> lg_sub;
+  for (int q = first; q <= last; ++q) {
+    const int32_t pg = pages[q];
+    if (pg < 0 || pg >= pool_pages) {
+      const int lo = max(0, (q << lg_sub) - first_tok);
+      const int hi = min(32, ((q + 1) << lg_sub) - first_tok);
+      const uint32_t m = (hi - lo >= 32) ? 0xFFFFFFFFu : (((1u << (hi - lo)) - 1u) << lo);
+      vis &= ~m;
+    }
+  }
+  return vis;
+}
+
 template <bool kFp8, int kAtoms>
 __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, const Item& it,
                                             uint32_t tbase, int tid) {
@@ -586,7 +599,8 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
     tc_fence_before();
     fence_proxy_async_smem();
     if (q_range) raise_status(p.status, DCP_STATUS_Q_RANGE);
-    mbar_arrive(&sh.bars[kBarQFull]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.bars[kBarQFull]);
   }
 
   const uint32_t peer = cta ^ 1;
@@ -604,88 +618,64 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
     return __all_sync(0xffffffffu,
                       wait_phase(&sh.bars[bar], parity, sh.abort_flag, p.status, cluster));
   };
-  // The two warps sharing rows (w and w^4) combine per-row values through smem,
-  // synchronised by an mbarrier per (lane quarter, parity) with bounded waits.
-  auto pair_sync = [&](int i) -> bool {
-    uint64_t* bar = &sh.bars[kBarComb + qw * 2 + (i & 1)];
-    mbar_arrive(bar);
-    return __all_sync(0xffffffffu, wait_phase(bar, (i >> 1) & 1, sh.abort_flag, p.status, false));
-  };
 
   const int n = it.n_tiles;
   float M = -INFINITY;  // running reference (log2 units), same in both CTAs
   float l_half = 0.f;   // sum of this half's weights
   bool ok = true;
   // own factors of the tile finished in the back half live in smem (registers are
-  // capped at 128 per thread with 14 warps): [half][group of 4][row] float4
+  // capped at 128 per thread with 15 warps): [half][group of 4][row] float4
   float4* eprev = reinterpret_cast<float4*>(sh.eprev) + h * 8 * kRows + r;
-  float m_prev = -INFINITY;
   int32_t pg_next = (big_pages && n > 0) ? __ldg(pages + (it.t_start >> lg_sub)) : 0;
   for (int i = 0; i <= n; ++i) {
     // ---------------- front: scores of tile i -> own factors -> peer
     float e_cur[32];
-    float m_cur = -INFINITY;
     if (i < n) {
       const int tok0 = it.t_start + i * kTileN;
       const int32_t pg_tile = pg_next;
-      if (!wait_warp(kBarSFullA, i & 1, false) || !wait_warp(kBarSFullB, i & 1, false)) {
+      if (!wait_warp(kBarSFull, i & 1, false)) {
         ok = false;
         break;
       }
       tc_fence_after();
 #pragma unroll
-      for (int half16 = 0; half16 < 2; ++half16) {
-        uint32_t sa[16], sb[16];
-        tmem_ld16(tSa + 16 * half16, sa);
-        tmem_ld16(tSb + 16 * half16, sb);
-        tmem_wait_ld16(sa);
-        tmem_wait_ld16(sb);
+      for (int q8 = 0; q8 < 4; ++q8) {
+        uint32_t sa[8], sb[8];
+        tmem_ld8(tSa + 8 * q8, sa);
+        tmem_ld8(tSb + 8 * q8, sb);
+        tmem_wait_ld8(sa);
+        tmem_wait_ld8(sb);
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          e_cur[16 * half16 + c] = __uint_as_float(sa[c]) + __uint_as_float(sb[c]);
+        for (int c = 0; c < 8; ++c)
+          e_cur[8 * q8 + c] = __uint_as_float(sa[c]) + __uint_as_float(sb[c]);
       }
       tc_fence_before();
-      mbar_arrive(&sh.bars[kBarSFree]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.bars[kBarSFree]);
       if (big_pages && i + 1 < n) pg_next = __ldg(pages + ((tok0 + kTileN) >> lg_sub));
       // visible tokens of this row in this half: [tok0 + 32h, row_end), pages valid
       const int cnt = max(0, min(32, row_end - tok0 - 32 * h));
       const bool page_ok = !big_pages || (pg_tile >= 0 && pg_tile < pool_pages);
-      // e_cur := 2^(x*sc - m*sc + 14) with x the raw partial score (sc > 0)
-      if (cnt == 32 && big_pages && page_ok) {
-        // every token visible (all but a row's last tile): no masking
-        float mx = e_cur[0];
+      // e_cur := 2^(x*sc - m*sc + 14) with x the raw partial score (sc > 0); masked
+      // tokens (past the row's boundary, invalid pages) become -inf, i.e. factor 0
+      uint32_t vis = cnt >= 32 ? 0xFFFFFFFFu : ((1u << cnt) - 1u);
+      if (!page_ok) vis = 0;
+      if (!big_pages && vis) vis = small_page_mask(vis, pages, tok0 + 32 * h, cnt, lg_sub, pool_pages);
+      if (vis != 0xFFFFFFFFu) {
 #pragma unroll
-        for (int c = 1; c < 32; ++c) mx = fmaxf(mx, e_cur[c]);
-        m_cur = mx * sc;
-        const float bias = kFactorLog2 - m_cur;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) e_cur[c] = fast_exp2(fmaf(e_cur[c], sc, bias));
-      } else {
-        uint32_t vis = cnt >= 32 ? 0xFFFFFFFFu : ((1u << cnt) - 1u);
-        if (!page_ok) vis = 0;
-        if (!big_pages && vis) {
-          const int first = (tok0 + 32 * h) >> lg_sub;
-          const int last = (tok0 + 32 * h + cnt - 1) >> lg_sub;
-          for (int q = first; q <= last; ++q) {
-            const int32_t pg = pages[q];
-            if (pg < 0 || pg >= pool_pages) {
-              const int lo = max(0, (q << lg_sub) - (tok0 + 32 * h));
-              const int hi = min(32, ((q + 1) << lg_sub) - (tok0 + 32 * h));
-              const uint32_t m = (hi - lo >= 32) ? 0xFFFFFFFFu : (((1u << (hi - lo)) - 1u) << lo);
-              vis &= ~m;
-            }
-          }
-        }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if ((vis >> c) & 1u) mx = fmaxf(mx, e_cur[c]);
-        m_cur = mx * sc;  // -inf if nothing is visible
-        const float bias = kFactorLog2 - m_cur;
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          e_cur[c] = ((vis >> c) & 1u) ? fast_exp2(fmaf(e_cur[c], sc, bias)) : 0.f;
+        for (int c = 0; c < 32; ++c) e_cur[c] = ((vis >> c) & 1u) ? e_cur[c] : -INFINITY;
       }
+      float m4[4] = {e_cur[0], e_cur[1], e_cur[2], e_cur[3]};
+#pragma unroll
+      for (int c = 4; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], e_cur[c]);
+      const float m_cur = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sc;  // -inf: none visible
+      const float bias = m_cur == -INFINITY ? 0.f : kFactorLog2 - m_cur;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) e_cur[c] = fast_exp2(fmaf(e_cur[c], sc, bias));
+      // own half maximum for the partner warp (same rows, other half)
+      sh.mown[((i % kMOwnBufs) * 2 + h) * kRows + r] = m_cur;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.bars[kBarMOwn + i % kMOwnBufs]);
       // send factors (f16 * 2^14) and m to the peer's slot i&1, free since tile i-2
       const int slot = i & 1;
       if (i >= 2 && !wait_warp(kBarXFree + slot, ((i >> 1) - 1) & 1, true)) {
@@ -716,22 +706,21 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
       const int slot = t & 1;
       // one thread arms this use of the slot with its size (the bytes may already be in)
       if (tid == 0) mbar_arrive_expect_tx(&sh.bars[kBarXFull + slot], kXchSlotBytes);
-      if (!wait_warp(kBarXFull + slot, (t >> 1) & 1, true)) {
+      if (!wait_warp(kBarXFull + slot, (t >> 1) & 1, true) ||
+          !wait_warp(kBarMOwn + t % kMOwnBufs, (t / kMOwnBufs) & 1, false)) {
         ok = false;
         break;
       }
       const uint8_t* src = sh.xch + slot * kXchSlotBytes;
-      const float m_peer = *reinterpret_cast<const float*>(src + kXchEBytes + (h * kRows + r) * 4);
-      // tile bound of the row (max over both halves of m_own + m_peer)
-      const float ub_h =
-          (m_prev == -INFINITY || m_peer == -INFINITY) ? -INFINITY : m_prev + m_peer;
-      float* comb = sh.comb + (t & 1) * 2 * kRows;
-      comb[h * kRows + r] = ub_h;
-      if (!pair_sync(t)) {
-        ok = false;
-        break;
-      }
-      const float ub = fmaxf(ub_h, comb[(h ^ 1) * kRows + r]);
+      const float* mpeer = reinterpret_cast<const float*>(src + kXchEBytes);
+      const float* mown = sh.mown + (t % kMOwnBufs) * 2 * kRows;
+      // tile bound of the row: max over both halves of m_own + m_peer
+      const float mo0 = mown[r], mo1 = mown[kRows + r];
+      const float mp0 = mpeer[r], mp1 = mpeer[kRows + r];
+      const float ub0 = (mo0 == -INFINITY || mp0 == -INFINITY) ? -INFINITY : mo0 + mp0;
+      const float ub1 = (mo1 == -INFINITY || mp1 == -INFINITY) ? -INFINITY : mo1 + mp1;
+      const float ub = fmaxf(ub0, ub1);
+      const float ub_h = h ? ub1 : ub0;
       const bool need = ub != -INFINITY && (M == -INFINITY || ub > M + kRescaleThreshold);
       float alpha = 1.f;
       if (need) {
@@ -739,7 +728,7 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
         l_half *= alpha;
         M = ub;
       }
-      // PV(t-1) done: P buffer is free and O is stable
+      // P.V(t-1) has completed: the P buffer is free and O is stable
       if (t >= 1 && !wait_warp(kBarODone, (t - 1) & 1, false)) {
         ok = false;
         break;
@@ -777,11 +766,13 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
         tmem_st4(tP + 4 * g, pk);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(xfree_remote + 8 * slot);  // done with the peer's slot
+      // done with the peer's slot: its values are in registers already
+      if (lane == 0) mbar_arrive_remote_relaxed(xfree_remote + 8 * slot);
       l_half += lsum;
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&sh.bars[kBarPFull]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.bars[kBarPFull]);
     }
     if (i < n) {
 #pragma unroll
@@ -789,17 +780,17 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
         eprev[g * kRows] =
             make_float4(e_cur[4 * g], e_cur[4 * g + 1], e_cur[4 * g + 2], e_cur[4 * g + 3]);
     }
-    m_prev = m_cur;
   }
 
   // epilogue: both halves' l, then this warp's 128 O columns of its rows
   const bool have_o =
       __all_sync(0xffffffffu, ok) && n > 0 && wait_warp(kBarODone, (n - 1) & 1, false);
   tc_fence_after();
-  float* comb = sh.comb + (n & 1) * 2 * kRows;
-  comb[h * kRows + r] = l_half;
-  const bool paired = pair_sync(n);
-  const float l_run = l_half + comb[(h ^ 1) * kRows + r];
+  sh.lcomb[h * kRows + r] = l_half;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&sh.bars[kBarLComb]);
+  const bool paired = wait_warp(kBarLComb, 0, false);
+  const float l_run = l_half + sh.lcomb[(h ^ 1) * kRows + r];
   const int64_t rh = (int64_t)it.b * qrows + qr;
   const int64_t base = ((int64_t)it.k * p.num_splits + it.s) * ((int64_t)R * p.H) + rh;
   const float inv = (paired && l_run > 0.f) ? kv_scale / l_run : 0.f;
@@ -823,21 +814,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sh.bars[kBarKvFull + i], 128);
-      mbar_init(&sh.bars[kBarKvEmpty + i], 2);
+      mbar_init(&sh.bars[kBarKvEmpty + i], 3);
     }
-    mbar_init(&sh.bars[kBarSFullA], 1);
-    mbar_init(&sh.bars[kBarSFullB], 1);
-    mbar_init(&sh.bars[kBarSFree], kSoftWarps * 32);
-    mbar_init(&sh.bars[kBarPFull], kSoftWarps * 32);
+    mbar_init(&sh.bars[kBarSFull], 2);
+    mbar_init(&sh.bars[kBarSFree], kSoftWarps);
+    mbar_init(&sh.bars[kBarPFull], kSoftWarps);
     mbar_init(&sh.bars[kBarODone], 1);
-    mbar_init(&sh.bars[kBarQFull], kSoftWarps * 32);
+    mbar_init(&sh.bars[kBarQFull], kSoftWarps);
     for (int i = 0; i < kXchSlots; ++i) {
       mbar_init(&sh.bars[kBarXFull + i], 1);  // armed by one local thread + the slot's bytes
       mbar_init(&sh.bars[kBarXFree + i], kSoftWarps);
     }
-    for (int i = 0; i < 8; ++i) mbar_init(&sh.bars[kBarComb + i], 64);
+    for (int i = 0; i < kMOwnBufs; ++i) mbar_init(&sh.bars[kBarMOwn + i], kSoftWarps);
+    mbar_init(&sh.bars[kBarLComb], kSoftWarps);
     mbar_init(&sh.bars[kBarDrainA], 1);
     mbar_init(&sh.bars[kBarDrainB], 1);
+    mbar_init(&sh.bars[kBarDrainP], 1);
     *sh.abort_flag = 0;
     fence_mbarrier_init_cluster();
     const int64_t sb = ((int64_t)it.k * p.batch + it.b) * p.num_splits + it.s;
@@ -862,11 +854,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (cta == 0) Producer<kFp8, 4>(p, sh, it, tid - kProdWarp0 * 32).run();
     else Producer<kFp8, 5>(p, sh, it, tid - kProdWarp0 * 32).run();
   } else if (tid == kMmaWarpA * 32) {
-    if (cta == 0) run_mma_a<kFp8, 4>(p, sh, it, tbase);
-    else run_mma_a<kFp8, 5>(p, sh, it, tbase);
+    // chain A: the first half of the k-steps (q atoms 0-1 from TMEM)
+    if (cta == 0) run_score_chain<kFp8, 4, 0, 8, kColSa, kBarDrainA>(p, sh, it, tbase);
+    else run_score_chain<kFp8, 5, 0, 10, kColSa, kBarDrainA>(p, sh, it, tbase);
   } else if (tid == kMmaWarpB * 32) {
-    if (cta == 0) run_mma_b<kFp8, 4>(p, sh, it, tbase);
-    else run_mma_b<kFp8, 5>(p, sh, it, tbase);
+    if (cta == 0) run_score_chain<kFp8, 4, 8, 16, kColSb, kBarDrainB>(p, sh, it, tbase);
+    else run_score_chain<kFp8, 5, 10, 20, kColSb, kBarDrainB>(p, sh, it, tbase);
+  } else if (tid == kMmaWarpP * 32) {
+    run_pv<kFp8>(p, sh, it, tbase);
   }
   tc_fence_before();
   __syncthreads();
