@@ -27,39 +27,38 @@
 //     error; each CTA normalises its own half of O by its own l.
 //   * CTA c stages dims [256c, 256c + 256 + 64c) of every token: its q.k slice,
 //     which also holds its value slice.
-//   * One thread issuing tcgen05.mma alone gets about one instruction per 280
-//     cycles whatever N is; two or three issuing warps each get about one per
-//     130-230 cycles (measured). So the q.k contraction is split into two chains
-//     of equal length with their own accumulators, and P.V has its own issuer:
-//     three issuing warps. The softmax adds the two partial scores.
+//   * A thread issuing straight-line tcgen05.mma gets about one instruction per
+//     55 (N=64) to 130 (N=256) cycles; branches or arithmetic between them were
+//     measured to double that. The whole q.k contraction is one straight-line
+//     chain (q from tensor memory), and P.V has its own issuing thread.
 //   * The factor exchange runs one tile behind: iteration i loads the scores of
 //     tile i and sends its factors, then finishes tile i-1 with the factors the
 //     peer sent an iteration earlier, so the exchange latency overlaps work.
-//     P.V has its own issuing warp and starts as soon as P is written, so the
-//     next P write (one iteration later) rarely waits for it.
+//     P.V starts as soon as P is written, so the next P write (one iteration
+//     later) rarely waits for it.
 //
-// Per CTA (480 threads):
+// Per CTA (448 threads):
 //   warps 0-7   softmax: warp w owns rows 32*(w%4) .. +31 (TMEM lane quarter)
-//               and token half w/4 of every 64-token tile; Q (TMEM + smem),
-//               factor exchange (double-buffered slots), lazy online softmax,
-//               P (16-bit) into TMEM, epilogue for O columns [128*(w/4), +128).
-//               The partner warp's half maximum comes through shared memory
-//               behind a per-tile barrier; a thread keeps its own factors of
-//               the previous tile in shared memory.
+//               and token half w/4 of every 64-token tile; Q into TMEM, factor
+//               exchange (double-buffered slots), lazy online softmax, P (16-bit)
+//               into TMEM, epilogue for O columns [128*(w/4), +128). The partner
+//               warp's half maximum comes through shared memory behind a per-tile
+//               barrier; a thread keeps its own factors of the previous tile in
+//               shared memory.
 //   warps 8-11  KV producers: 16-byte loads of the paged cache rows (subpage ids
-//               from the metadata, bounds-checked, two tiles in flight), FP8
-//               E4M3 -> f16 conversion, stores into 128-byte-swizzled K-major
-//               tiles of a 3-stage ring.
-//   warp 12     TMEM allocation; one thread issues score chain A (k-steps
-//               [0, K/2): q atoms 0-2 from TMEM, the rest from shared memory).
-//   warp 13     one thread issues score chain B (k-steps [K/2, K), q from smem).
-//   warp 14     one thread issues O += P[tmem] . V_tile (M=128, N=256, V read
+//               from the metadata, bounds-checked), FP8 E4M3 -> f16 conversion,
+//               stores into 128-byte-swizzled K-major tiles of a 3-stage ring.
+//               A tile's loads are issued right after the previous tile is
+//               stored, so they fly while the producer waits for a free stage.
+//   warp 12     TMEM allocation; one thread issues S = Q[tmem] . K_tile^T
+//               (M=128, N=64, all of this CTA's dims).
+//   warp 13     one thread issues O += P[tmem] . V_tile (M=128, N=256, V read
 //               MN-major from the same swizzled tile as K).
-// TMEM columns: O [0,256), S_a [256,320), S_b [320,384), P [384,416),
-// Q atoms 0-2 [416,512). The FP8-cache path computes in f16
-// (E4M3 -> f16 is exact; q is BF16 -> f16, exact in f16's normal range;
-// |q| > 65504 sets DCP_STATUS_Q_RANGE); the BF16-cache path computes in bf16.
-// Accumulation is fp32 throughout.
+// TMEM columns: O [0,256), S [256,320), P [320,352), Q [352,512) (CTA1: five
+// 64-dim atoms, CTA0: four). The FP8-cache path computes in f16 (E4M3 -> f16
+// is exact; q is BF16 -> f16, exact in f16's normal range; |q| > 65504 sets
+// DCP_STATUS_Q_RANGE); the BF16-cache path computes in bf16. Accumulation is
+// fp32 throughout.
 //
 // Every wait is bounded (DCP_STATUS_TIMEOUT and an orderly exit: all roles stop,
 // in-flight MMAs are drained, TMEM is freed). Waiting threads sleep in
@@ -83,8 +82,6 @@ constexpr int kMaxAtoms = 5;   // 64-dim swizzle atoms staged per CTA (CTA1: 320
 constexpr int kAtomBytes = kTileN * 128;
 constexpr int kStageBytes = kMaxAtoms * kAtomBytes;
 constexpr int kQAtomBytes = kRows * 128;       // one 64-dim atom of Q (128 rows)
-constexpr int kQTmemAtoms = 3;                 // q atoms 0..2 live in TMEM, 3.. in smem
-constexpr int kQSmemBytes = (kMaxAtoms - kQTmemAtoms) * kQAtomBytes;
 // factor exchange slot: E as f16 [half 2][group 4][row 128][8 values], m as f32 [half][row]
 constexpr int kXchEBytes = 2 * 4 * kRows * 16;
 constexpr int kXchSlotBytes = kXchEBytes + 2 * kRows * 4;
@@ -95,11 +92,10 @@ constexpr int kLCombBytes = 2 * kRows * 4;              // [half][row] f32, epil
 constexpr int kEPrevBytes = 2 * kTileN / 2 * kRows * 4;  // own fp32 factors [half][32][row]
 constexpr int kSoftWarps = 8;
 constexpr int kProdWarp0 = 8;
-constexpr int kMmaWarpA = 12;
-constexpr int kMmaWarpB = 13;
-constexpr int kMmaWarpP = 14;
-constexpr int kThreads = 15 * 32;
-constexpr uint32_t kColO = 0, kColSa = 256, kColSb = 320, kColP = 384, kColQ = 416;
+constexpr int kMmaWarpS = 12;
+constexpr int kMmaWarpP = 13;
+constexpr int kThreads = 14 * 32;
+constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // P may grow to 2^8 before O is rescaled
 constexpr float kFactorLog2 = 14.0f;       // factors carry 2^14: E down to 2^-28 stays normal in f16
@@ -110,8 +106,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 // barrier slots
 enum {
   kBarKvFull = 0,
-  kBarKvEmpty = kBarKvFull + kStages,  // count 3: chain A, chain B, P.V
-  kBarSFull = kBarKvEmpty + kStages,   // count 2: chain A, chain B
+  kBarKvEmpty = kBarKvFull + kStages,  // count 2: score chain, P.V
+  kBarSFull = kBarKvEmpty + kStages,   // score chain committed
   kBarSFree,                           // count 8: softmax warps read S
   kBarPFull,                           // count 8: P written
   kBarODone,                           // P.V completed
@@ -120,13 +116,12 @@ enum {
   kBarXFree = kBarXFull + kXchSlots,   // [2] count 8: the peer consumed what I wrote
   kBarMOwn = kBarXFree + kXchSlots,    // [3] count 8: own half maxima of a tile written
   kBarLComb = kBarMOwn + kMOwnBufs,    // count 8: epilogue l halves written
-  kBarDrainA,
-  kBarDrainB,
+  kBarDrainS,
   kBarDrainP,
   kNumBars
 };
 
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kQSmemBytes +
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes +
                               kXchSlots * kXchSlotBytes + kMOwnBytes + kLCombBytes +
                               kEPrevBytes + kNumBars * 8 + 16;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -150,7 +145,6 @@ struct Params {
 
 struct Shared {
   uint8_t* stages;
-  uint8_t* qs;    // Q atoms kQTmemAtoms.. (shared-memory operand)
   uint8_t* xch;   // kXchSlots slots
   float* mown;    // own half maxima per tile
   float* lcomb;   // epilogue l halves
@@ -165,8 +159,7 @@ __device__ __forceinline__ Shared carve(unsigned char* raw) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   s.stages = base;
-  s.qs = base + kStages * kStageBytes;
-  s.xch = s.qs + kQSmemBytes;
+  s.xch = base + kStages * kStageBytes;
   s.mown = reinterpret_cast<float*>(s.xch + kXchSlots * kXchSlotBytes);
   s.lcomb = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s.mown) + kMOwnBytes);
   s.eprev = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s.lcomb) + kLCombBytes);
@@ -366,29 +359,17 @@ struct Producer {
     return true;
   }
 
-  // FP8: two register buffers, so tile i+1's loads are in flight while tile i is
-  // converted and stored; tile pages are read one tile ahead. BF16 (twice the
-  // registers per tile): one buffer. One call site each keeps the code small.
+  // One register buffer: tile i+1's loads are issued right after tile i is stored,
+  // so they are in flight while this thread waits for the next free stage (the
+  // ring runs ahead of the consumers, so that wait is long).
   __device__ __forceinline__ void run() {
     const int n = it.n_tiles;
-    if (kFp8) {
-      uint4 va[kLoads], vb[kLoads];
-      int32_t pg_next = tile_page(1);
-      load(0, tile_page(0), va);
-      for (int i = 0; i < n; ++i) {
-        const int32_t pg = pg_next;
-        pg_next = tile_page(i + 2);
-        if (i + 1 < n) load(i + 1, pg, vb);
-        if (!store(i, va)) break;
-#pragma unroll
-        for (int l = 0; l < kLoads; ++l) va[l] = vb[l];
-      }
-    } else {
-      uint4 v[kLoads];
-      for (int i = 0; i < n; ++i) {
-        load(i, tile_page(i), v);
-        if (!store(i, v)) break;
-      }
+    uint4 v[kLoads];
+    if (n > 0) load(0, tile_page(0), v);
+    for (int i = 0; i < n; ++i) {
+      const int32_t pg_next = tile_page(i + 1);
+      if (!store(i, v)) break;
+      if (i + 1 < n) load(i + 1, pg_next, v);
     }
     if (bad_page) raise_status(p.status, DCP_STATUS_BAD_PAGE);
   }
@@ -401,15 +382,13 @@ struct Producer {
 // straight line whose descriptors are per-tile bases plus constants (the
 // address field of a descriptor is the byte address / 16 in its low bits).
 
-// Score chain over k-steps [KK0, KK1) of this CTA's 4*kAtoms (16 dims each) into
-// the accumulator at column kAcc. q atoms 0..kQTmemAtoms-1 come from TMEM, the
-// rest from shared memory.
-template <bool kFp8, int kAtoms, int KK0, int KK1, uint32_t kAcc, int kDrainBar>
+// The score chain: S = Q . K_tile^T over this CTA's 4*kAtoms k-steps (16 dims
+// each), q from TMEM, K from the stage (K-major, 128-byte swizzle).
+template <bool kFp8, int kAtoms>
 __device__ __forceinline__ void run_score_chain(const Params& p, const Shared& sh, const Item& it,
                                                 uint32_t tbase) {
   constexpr uint32_t idq = idesc_f16(kRows, kTileN, !kFp8, false);
   const uint32_t stage0 = smem_u32(sh.stages);
-  const uint64_t qdesc0 = smem_desc_sw128(smem_u32(sh.qs), 16, 1024);
   if (wait_phase(&sh.bars[kBarQFull], 0, sh.abort_flag, p.status, false)) {
     tc_fence_after();
     for (int i = 0; i < it.n_tiles; ++i) {
@@ -422,25 +401,18 @@ __device__ __forceinline__ void run_score_chain(const Params& p, const Shared& s
       tc_fence_after();
       const uint64_t bdesc0 = smem_desc_sw128(stage0 + st * kStageBytes, 16, 1024);
 #pragma unroll
-      for (int kk = KK0; kk < KK1; ++kk) {
-        const uint64_t b = bdesc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
-        const uint32_t acc = kk > KK0 ? 1u : 0u;
-        if ((kk >> 2) < kQTmemAtoms) {
-          mma_f16_ts(tbase + kAcc, tbase + kColQ + 8 * kk, b, idq, acc);
-        } else {
-          const uint64_t a =
-              qdesc0 + (uint64_t)((((kk >> 2) - kQTmemAtoms) * kQAtomBytes + (kk & 3) * 32) >> 4);
-          mma_f16_ss(tbase + kAcc, a, b, idq, acc);
-        }
-      }
+      for (int kk = 0; kk < 4 * kAtoms; ++kk)
+        mma_f16_ts(tbase + kColS, tbase + kColQ + 8 * kk,
+                   bdesc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idq,
+                   kk > 0 ? 1u : 0u);
       tc_commit(&sh.bars[kBarSFull]);
       tc_commit(&sh.bars[kBarKvEmpty + st]);
     }
   }
   // drain: every MMA issued above has completed before TMEM can be released
-  tc_commit(&sh.bars[kDrainBar]);
+  tc_commit(&sh.bars[kBarDrainS]);
   int never = 0;
-  wait_phase(&sh.bars[kDrainBar], 0, &never, p.status, false);
+  wait_phase(&sh.bars[kBarDrainS], 0, &never, p.status, false);
 }
 
 // O += P(j) . V(j) for every tile, as soon as the softmax has written P(j).
@@ -507,15 +479,14 @@ __device__ __noinline__ void store_o(uint32_t tO, bool have_o, bool row_ok, floa
   }
 }
 
-// Q slice of one row: atoms 0..kQTmemAtoms-1 -> TMEM, the rest -> smem (swizzled
-// K-major); half 0 loads the TMEM atoms, half 1 the rest. Returns true if some
-// |q| exceeds the f16 range on the FP8 path.
+// Q slice of one row into TMEM (16-bit, 2 per column; atom a at columns 32a);
+// half 0 loads atoms 0-2, half 1 the rest. Returns true if some |q| exceeds the
+// f16 range on the FP8 path.
 template <bool kFp8, int kAtoms>
-__device__ __noinline__ bool load_q(const uint16_t* src, bool row_ok, int h, int r, uint32_t tQ,
-                                    uint8_t* qs) {
+__device__ __noinline__ bool load_q(const uint16_t* src, bool row_ok, int h, uint32_t tQ) {
   bool q_range = false;
-  const int a0 = h == 0 ? 0 : kQTmemAtoms;
-  const int a1 = h == 0 ? kQTmemAtoms : kAtoms;
+  const int a0 = h == 0 ? 0 : 3;
+  const int a1 = h == 0 ? 3 : kAtoms;
   for (int a = a0; a < a1; ++a) {
     uint32_t w[32];
 #pragma unroll
@@ -536,15 +507,7 @@ __device__ __noinline__ bool load_q(const uint16_t* src, bool row_ok, int h, int
         }
       }
     }
-    if (a < kQTmemAtoms) {
-      tmem_st32(tQ + 32 * a, w);
-    } else {
-      uint8_t* at = qs + (a - kQTmemAtoms) * kQAtomBytes;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(at + sw128_offset(r, c)) =
-            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-    }
+    tmem_st32(tQ + 32 * a, w);
   }
   tmem_wait_st();
   return q_range;
@@ -578,8 +541,7 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
   const int h = warp >> 2;   // token half of each tile / O column half
   const int r = qw * 32 + lane;
   const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-  const uint32_t tSa = tbase + lane_off + kColSa + 32 * h;
-  const uint32_t tSb = tbase + lane_off + kColSb + 32 * h;
+  const uint32_t tS = tbase + lane_off + kColS + 32 * h;
   const uint32_t tP = tbase + lane_off + kColP + 16 * h;
   const uint32_t tO = tbase + lane_off + kColO + 128 * h;
   const uint32_t tQ = tbase + lane_off + kColQ;
@@ -595,9 +557,8 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
 
   {
     const uint16_t* src = p.q + ((int64_t)it.b * qrows + qr) * kDqk + d0;
-    const bool q_range = load_q<kFp8, kAtoms>(src, row_ok, h, r, tQ, sh.qs);
+    const bool q_range = load_q<kFp8, kAtoms>(src, row_ok, h, tQ);
     tc_fence_before();
-    fence_proxy_async_smem();
     if (q_range) raise_status(p.status, DCP_STATUS_Q_RANGE);
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.bars[kBarQFull]);
@@ -638,16 +599,12 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
         break;
       }
       tc_fence_after();
+      {
+        uint32_t sv[32];
+        tmem_ld32(tS, sv);
+        tmem_wait_ld(sv);
 #pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        uint32_t sa[8], sb[8];
-        tmem_ld8(tSa + 8 * q8, sa);
-        tmem_ld8(tSb + 8 * q8, sb);
-        tmem_wait_ld8(sa);
-        tmem_wait_ld8(sb);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          e_cur[8 * q8 + c] = __uint_as_float(sa[c]) + __uint_as_float(sb[c]);
+        for (int c = 0; c < 32; ++c) e_cur[c] = __uint_as_float(sv[c]);
       }
       tc_fence_before();
       __syncwarp();
@@ -814,9 +771,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sh.bars[kBarKvFull + i], 128);
-      mbar_init(&sh.bars[kBarKvEmpty + i], 3);
+      mbar_init(&sh.bars[kBarKvEmpty + i], 2);
     }
-    mbar_init(&sh.bars[kBarSFull], 2);
+    mbar_init(&sh.bars[kBarSFull], 1);
     mbar_init(&sh.bars[kBarSFree], kSoftWarps);
     mbar_init(&sh.bars[kBarPFull], kSoftWarps);
     mbar_init(&sh.bars[kBarODone], 1);
@@ -827,8 +784,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kMOwnBufs; ++i) mbar_init(&sh.bars[kBarMOwn + i], kSoftWarps);
     mbar_init(&sh.bars[kBarLComb], kSoftWarps);
-    mbar_init(&sh.bars[kBarDrainA], 1);
-    mbar_init(&sh.bars[kBarDrainB], 1);
+    mbar_init(&sh.bars[kBarDrainS], 1);
     mbar_init(&sh.bars[kBarDrainP], 1);
     *sh.abort_flag = 0;
     fence_mbarrier_init_cluster();
@@ -837,7 +793,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (cta == 0 && it.t == 0 && (beg < 0 || end < beg || end > p.max_pages))
       raise_status(p.status, DCP_STATUS_BAD_SPLIT);
   }
-  if (warp == kMmaWarpA) {
+  if (warp == kMmaWarpS) {
     tmem_alloc(sh.tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -850,23 +806,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp < kSoftWarps) {
     if (cta == 0) run_softmax<kFp8, 4>(p, sh, it, tbase, tid);
     else run_softmax<kFp8, 5>(p, sh, it, tbase, tid);
-  } else if (warp < kMmaWarpA) {
+  } else if (warp < kMmaWarpS) {
     if (cta == 0) Producer<kFp8, 4>(p, sh, it, tid - kProdWarp0 * 32).run();
     else Producer<kFp8, 5>(p, sh, it, tid - kProdWarp0 * 32).run();
-  } else if (tid == kMmaWarpA * 32) {
-    // chain A: the first half of the k-steps (q atoms 0-1 from TMEM)
-    if (cta == 0) run_score_chain<kFp8, 4, 0, 8, kColSa, kBarDrainA>(p, sh, it, tbase);
-    else run_score_chain<kFp8, 5, 0, 10, kColSa, kBarDrainA>(p, sh, it, tbase);
-  } else if (tid == kMmaWarpB * 32) {
-    if (cta == 0) run_score_chain<kFp8, 4, 8, 16, kColSb, kBarDrainB>(p, sh, it, tbase);
-    else run_score_chain<kFp8, 5, 10, 20, kColSb, kBarDrainB>(p, sh, it, tbase);
+  } else if (tid == kMmaWarpS * 32) {
+    if (cta == 0) run_score_chain<kFp8, 4>(p, sh, it, tbase);
+    else run_score_chain<kFp8, 5>(p, sh, it, tbase);
   } else if (tid == kMmaWarpP * 32) {
     run_pv<kFp8>(p, sh, it, tbase);
   }
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // the peer no longer touches this CTA's shared memory
-  if (warp == kMmaWarpA) {
+  if (warp == kMmaWarpS) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
