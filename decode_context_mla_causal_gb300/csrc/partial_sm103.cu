@@ -100,7 +100,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // P may grow to 2^8 before O is rescaled
 constexpr float kFactorLog2 = 14.0f;       // factors carry 2^14: E down to 2^-28 stays normal in f16
 constexpr uint64_t kTimeoutNs = 4000000000ull;
-constexpr uint64_t kPollNs = 20000;  // poll this long before sleeping in a wait
 constexpr float kLog2e = 1.4426950408889634f;
 
 // barrier slots
@@ -169,34 +168,29 @@ __device__ __forceinline__ Shared carve(unsigned char* raw) {
   return s;
 }
 
-// Bounded wait on an mbarrier phase. The slow path polls try_wait for a few
-// microseconds (a suspended waiter was measured to wake up to ~0.5 us late),
-// then sleeps in try_wait with a suspend-time hint; it gives up after
-// kTimeoutNs (raising the abort flag and DCP_STATUS_TIMEOUT), and returns false
-// at once when another thread of the CTA has already aborted.
+// Bounded wait on an mbarrier phase. try_wait with a suspend-time hint was
+// measured to notice a completed phase ~170 cycles after the arrive (a plain
+// try_wait: ~280), so every attempt carries the hint; between attempts the slow
+// path checks the abort flag and gives up after kTimeoutNs (raising the abort
+// flag and DCP_STATUS_TIMEOUT).
 __device__ __noinline__ bool wait_phase_slow(uint32_t a, uint32_t parity, int* abort_flag,
                                              uint32_t* status, bool cluster_acquire) {
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (cluster_acquire ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
-    if ((it & 31u) == 0) {
-      const uint64_t dt = globaltimer_ns() - t0;
-      if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
-      if (dt > kTimeoutNs) {
-        *reinterpret_cast<volatile int*>(abort_flag) = 1;
-        raise_status(status, DCP_STATUS_TIMEOUT);
-        return false;
-      }
-      if (dt > kPollNs &&
-          (cluster_acquire ? mbar_wait_sleep_cluster(a, parity) : mbar_wait_sleep(a, parity)))
-        return true;
+  for (;;) {
+    if (cluster_acquire ? mbar_wait_sleep_cluster(a, parity) : mbar_wait_sleep(a, parity))
+      return true;
+    if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
+    if (globaltimer_ns() - t0 > kTimeoutNs) {
+      *reinterpret_cast<volatile int*>(abort_flag) = 1;
+      raise_status(status, DCP_STATUS_TIMEOUT);
+      return false;
     }
   }
 }
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, int* abort_flag,
                                            uint32_t* status, bool cluster_acquire) {
   const uint32_t a = smem_u32(bar);
-  if (cluster_acquire ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
+  if (cluster_acquire ? mbar_wait_sleep_cluster(a, parity) : mbar_wait_sleep(a, parity)) return true;
   return wait_phase_slow(a, parity, abort_flag, status, cluster_acquire);
 }
 

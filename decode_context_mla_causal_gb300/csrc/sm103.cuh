@@ -61,7 +61,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t pa
 
 // try_wait that may suspend the thread (up to the hint, in ns) until the phase
 // completes, so waiting warps do not take issue slots.
-constexpr uint32_t kSuspendHintNs = 100000;
+constexpr uint32_t kSuspendHintNs = 20000;
 __device__ __forceinline__ bool mbar_wait_sleep(uint32_t addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
