@@ -50,10 +50,12 @@
 //               stores into 128-byte-swizzled K-major tiles of a 3-stage ring.
 //               A tile's loads are issued right after the previous tile is
 //               stored, so they fly while the producer waits for a free stage.
-//   warp 12     TMEM allocation; one thread issues S = Q[tmem] . K_tile^T
-//               (M=128, N=64, all of this CTA's dims).
-//   warp 13     one thread issues O += P[tmem] . V_tile (M=128, N=256, V read
-//               MN-major from the same swizzled tile as K).
+//   warp 12     TMEM allocation; issues S = Q[tmem] . K_tile^T (M=128, N=64, all
+//               of this CTA's dims).
+//   warp 13     issues O += P[tmem] . V_tile (M=128, N=256, V read MN-major from
+//               the same swizzled tile as K).
+//   The issuing warps run converged and one elected lane issues each tcgen05
+//   instruction, so its operands are warp-uniform values.
 // TMEM columns: O [0,256), S [256,320), P [320,352), Q [352,512) (CTA1: five
 // 64-dim atoms, CTA0: four). The FP8-cache path computes in f16 (E4M3 -> f16
 // is exact; q is BF16 -> f16, exact in f16's normal range; |q| > 65504 sets
@@ -192,6 +194,13 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, int* 
   const uint32_t a = smem_u32(bar);
   if (cluster_acquire ? mbar_wait_sleep_cluster(a, parity) : mbar_wait_sleep(a, parity)) return true;
   return wait_phase_slow(a, parity, abort_flag, status, cluster_acquire);
+}
+
+// wait_phase for a whole converged warp, with a warp-uniform result (the
+// elect.sync of the tcgen05 issue that follows needs every lane).
+__device__ __forceinline__ bool wait_uniform(uint64_t* bar, uint32_t parity, int* abort_flag,
+                                             uint32_t* status) {
+  return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, status, false));
 }
 
 struct Item {
@@ -383,30 +392,29 @@ __device__ __forceinline__ void run_score_chain(const Params& p, const Shared& s
                                                 uint32_t tbase) {
   constexpr uint32_t idq = idesc_f16(kRows, kTileN, !kFp8, false);
   const uint32_t stage0 = smem_u32(sh.stages);
-  if (wait_phase(&sh.bars[kBarQFull], 0, sh.abort_flag, p.status, false)) {
+  if (wait_uniform(&sh.bars[kBarQFull], 0, sh.abort_flag, p.status)) {
     tc_fence_after();
     for (int i = 0; i < it.n_tiles; ++i) {
       const int st = i % kStages;
-      if (!wait_phase(&sh.bars[kBarKvFull + st], (i / kStages) & 1, sh.abort_flag, p.status,
-                      false))
+      if (!wait_uniform(&sh.bars[kBarKvFull + st], (i / kStages) & 1, sh.abort_flag, p.status))
         break;
-      if (i >= 1 && !wait_phase(&sh.bars[kBarSFree], (i - 1) & 1, sh.abort_flag, p.status, false))
+      if (i >= 1 && !wait_uniform(&sh.bars[kBarSFree], (i - 1) & 1, sh.abort_flag, p.status))
         break;
       tc_fence_after();
       const uint64_t bdesc0 = smem_desc_sw128(stage0 + st * kStageBytes, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < 4 * kAtoms; ++kk)
-        mma_f16_ts(tbase + kColS, tbase + kColQ + 8 * kk,
-                   bdesc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idq,
-                   kk > 0 ? 1u : 0u);
-      tc_commit(&sh.bars[kBarSFull]);
-      tc_commit(&sh.bars[kBarKvEmpty + st]);
+        mma_f16_ts_elect(tbase + kColS, tbase + kColQ + 8 * kk,
+                         bdesc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idq,
+                         kk > 0 ? 1u : 0u);
+      tc_commit_elect(&sh.bars[kBarSFull]);
+      tc_commit_elect(&sh.bars[kBarKvEmpty + st]);
     }
   }
   // drain: every MMA issued above has completed before TMEM can be released
-  tc_commit(&sh.bars[kBarDrainS]);
+  tc_commit_elect(&sh.bars[kBarDrainS]);
   int never = 0;
-  wait_phase(&sh.bars[kBarDrainS], 0, &never, p.status, false);
+  wait_uniform(&sh.bars[kBarDrainS], 0, &never, p.status);
 }
 
 // O += P(j) . V(j) for every tile, as soon as the softmax has written P(j).
@@ -416,21 +424,21 @@ __device__ __forceinline__ void run_pv(const Params& p, const Shared& sh, const 
   constexpr uint32_t idp = idesc_f16(kRows, 256, !kFp8, true);
   const uint32_t stage0 = smem_u32(sh.stages);
   for (int j = 0; j < it.n_tiles; ++j) {
-    if (!wait_phase(&sh.bars[kBarPFull], j & 1, sh.abort_flag, p.status, false)) break;
+    if (!wait_uniform(&sh.bars[kBarPFull], j & 1, sh.abort_flag, p.status)) break;
     tc_fence_after();
     const uint64_t vdesc0 = smem_desc_sw128(stage0 + (j % kStages) * kStageBytes, kAtomBytes, 1024);
     const uint32_t tp = tbase + kColP;
     const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk)
-      mma_f16_ts(tbase + kColO, tp + 8 * kk, vdesc0 + (uint64_t)((kk * 2048) >> 4), idp,
-                 kk > 0 ? 1u : acc0);
-    tc_commit(&sh.bars[kBarODone]);
-    tc_commit(&sh.bars[kBarKvEmpty + (j % kStages)]);
+      mma_f16_ts_elect(tbase + kColO, tp + 8 * kk, vdesc0 + (uint64_t)((kk * 2048) >> 4), idp,
+                       kk > 0 ? 1u : acc0);
+    tc_commit_elect(&sh.bars[kBarODone]);
+    tc_commit_elect(&sh.bars[kBarKvEmpty + (j % kStages)]);
   }
-  tc_commit(&sh.bars[kBarDrainP]);
+  tc_commit_elect(&sh.bars[kBarDrainP]);
   int never = 0;
-  wait_phase(&sh.bars[kBarDrainP], 0, &never, p.status, false);
+  wait_uniform(&sh.bars[kBarDrainP], 0, &never, p.status);
 }
 
 // ----------------------------------------------------------------- softmax
@@ -527,10 +535,10 @@ __device__ __noinline__ uint32_t small_page_mask(uint32_t vis, const int32_t* pa
 
 template <bool kFp8, int kAtoms>
 __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, const Item& it,
-                                            uint32_t tbase, int tid) {
+                                            uint32_t tbase, int tid, int warp) {
   constexpr int cta = kAtoms - 4;
   constexpr int d0 = 256 * cta;
-  const int warp = tid >> 5, lane = tid & 31;
+  const int lane = tid & 31;
   const int qw = warp & 3;   // TMEM lane quarter
   const int h = warp >> 2;   // token half of each tile / O column half
   const int r = qw * 32 + lane;
@@ -758,7 +766,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   extern __shared__ unsigned char smem_raw[];
   const Shared sh = carve(smem_raw);
   const int tid = threadIdx.x;
-  const int warp = tid >> 5;
+  // warp-uniform by construction (the shuffle tells the compiler so): TMEM and
+  // tcgen05 operands derived from it need no per-lane serialisation
+  const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
   const int cta = (int)cluster_ctarank();
   const Item it = decode_item(p, blockIdx.x >> 1);
 
@@ -795,18 +805,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   cluster_sync_all();
   tc_fence_after();
-  const uint32_t tbase = *sh.tmem_slot;
+  const uint32_t tbase = __shfl_sync(0xffffffffu, *sh.tmem_slot, 0);
 
   if (warp < kSoftWarps) {
-    if (cta == 0) run_softmax<kFp8, 4>(p, sh, it, tbase, tid);
-    else run_softmax<kFp8, 5>(p, sh, it, tbase, tid);
+    if (cta == 0) run_softmax<kFp8, 4>(p, sh, it, tbase, tid, warp);
+    else run_softmax<kFp8, 5>(p, sh, it, tbase, tid, warp);
   } else if (warp < kMmaWarpS) {
     if (cta == 0) Producer<kFp8, 4>(p, sh, it, tid - kProdWarp0 * 32).run();
     else Producer<kFp8, 5>(p, sh, it, tid - kProdWarp0 * 32).run();
-  } else if (tid == kMmaWarpS * 32) {
+  } else if (warp == kMmaWarpS) {
     if (cta == 0) run_score_chain<kFp8, 4>(p, sh, it, tbase);
     else run_score_chain<kFp8, 5>(p, sh, it, tbase);
-  } else if (tid == kMmaWarpP * 32) {
+  } else if (warp == kMmaWarpP) {
     run_pv<kFp8>(p, sh, it, tbase);
   }
   tc_fence_before();
