@@ -48,8 +48,8 @@
 //   warps 8-11  KV producers: 16-byte loads of the paged cache rows (subpage ids
 //               from the metadata, bounds-checked), FP8 E4M3 -> f16 conversion,
 //               stores into 128-byte-swizzled K-major tiles of a 3-stage ring.
-//               A tile's loads are issued right after the previous tile is
-//               stored, so they fly while the producer waits for a free stage.
+//               FP8 keeps two tiles in flight (registers + cp.async staging in
+//               shared memory), so a freed stage only waits for the conversion.
 //   warp 12     TMEM allocation; issues S = Q[tmem] . K_tile^T (M=128, N=64, all
 //               of this CTA's dims).
 //   warp 13     issues O += P[tmem] . V_tile (M=128, N=256, V read MN-major from
@@ -92,6 +92,9 @@ constexpr int kMOwnBufs = 3;                            // own half maxima, by t
 constexpr int kMOwnBytes = kMOwnBufs * 2 * kRows * 4;   // [tile%3][half][row] f32
 constexpr int kLCombBytes = 2 * kRows * 4;              // [half][row] f32, epilogue
 constexpr int kEPrevBytes = 2 * kTileN / 2 * kRows * 4;  // own fp32 factors [half][32][row]
+// FP8 producer staging: each producer thread's 16-byte chunks of one tile (the
+// tile after next), [chunk][thread], written by cp.async
+constexpr int kRawBytes = kMaxAtoms * 2 * 128 * 16;
 constexpr int kSoftWarps = 8;
 constexpr int kProdWarp0 = 8;
 constexpr int kMmaWarpS = 12;
@@ -124,7 +127,7 @@ enum {
 
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes +
                               kXchSlots * kXchSlotBytes + kMOwnBytes + kLCombBytes +
-                              kEPrevBytes + kNumBars * 8 + 16;
+                              kEPrevBytes + kRawBytes + kNumBars * 8 + 16;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct Params {
@@ -150,6 +153,7 @@ struct Shared {
   float* mown;    // own half maxima per tile
   float* lcomb;   // epilogue l halves
   float* eprev;   // own factors of the tile awaiting the peer's
+  uint8_t* raw;   // FP8 producer staging
   uint64_t* bars;
   uint32_t* tmem_slot;
   int* abort_flag;
@@ -164,7 +168,8 @@ __device__ __forceinline__ Shared carve(unsigned char* raw) {
   s.mown = reinterpret_cast<float*>(s.xch + kXchSlots * kXchSlotBytes);
   s.lcomb = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s.mown) + kMOwnBytes);
   s.eprev = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s.lcomb) + kLCombBytes);
-  s.bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.eprev) + kEPrevBytes);
+  s.raw = reinterpret_cast<uint8_t*>(s.eprev) + kEPrevBytes;
+  s.bars = reinterpret_cast<uint64_t*>(s.raw + kRawBytes);
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + kNumBars);
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
   return s;
@@ -302,9 +307,9 @@ struct Producer {
     return __ldg(pages + ((it.t_start + i * kTileN) >> lg_sub));
   }
 
-  __device__ __forceinline__ void load(int i, int32_t pg_tile, uint4 (&v)[kLoads]) {
+  // Row pointers of this thread's tokens of tile i (nullptr: masked or invalid page).
+  __device__ __forceinline__ void rows(int i, int32_t pg_tile, const uint8_t* (&rp)[kToks]) {
     const int tok0 = it.t_start + i * kTileN + tk0;
-    const uint8_t* rp[kToks];
 #pragma unroll
     for (int j = 0; j < kToks; ++j) {
       const int li = tok0 + j * kTokStride;
@@ -319,6 +324,32 @@ struct Producer {
         }
       }
     }
+  }
+
+  // cp.async of this thread's chunks of tile i into its staging slots (chunk l
+  // at raw + l*2048 + ct*16); masked chunks are zero-filled.
+  __device__ __forceinline__ void issue(int i, int32_t pg_tile, uint32_t raw) {
+    const uint8_t* rp[kToks];
+    rows(i, pg_tile, rp);
+#pragma unroll
+    for (int a = 0; a < kAtoms; ++a)
+#pragma unroll
+      for (int j = 0; j < kToks; ++j)
+        cp_async16(raw + (a * kToks + j) * 2048, rp[j] ? rp[j] + a * 64 * kElem : pool,
+                   rp[j] ? 16u : 0u);
+    cp_async_commit();
+  }
+
+  // Staged tile -> registers (waits for this thread's copies).
+  __device__ __forceinline__ void fetch(const uint8_t* raw, uint4 (&v)[kLoads]) {
+    cp_async_wait_all();
+#pragma unroll
+    for (int l = 0; l < kLoads; ++l) v[l] = *reinterpret_cast<const uint4*>(raw + l * 2048);
+  }
+
+  __device__ __forceinline__ void load(int i, int32_t pg_tile, uint4 (&v)[kLoads]) {
+    const uint8_t* rp[kToks];
+    rows(i, pg_tile, rp);
 #pragma unroll
     for (int a = 0; a < kAtoms; ++a)
 #pragma unroll
@@ -362,17 +393,37 @@ struct Producer {
     return true;
   }
 
-  // One register buffer: tile i+1's loads are issued right after tile i is stored,
-  // so they are in flight while this thread waits for the next free stage (the
-  // ring runs ahead of the consumers, so that wait is long).
-  __device__ __forceinline__ void run() {
+  // FP8: two tiles in flight. Registers hold tile i+1 and the shared staging
+  // slots receive tile i+2 (cp.async) while this thread waits for a free stage,
+  // so a freed stage is refilled by the conversion alone. BF16 (twice the bytes,
+  // no room to stage): one register buffer, loaded right after the previous store.
+  __device__ __forceinline__ void run(int ct) {
     const int n = it.n_tiles;
     uint4 v[kLoads];
-    if (n > 0) load(0, tile_page(0), v);
-    for (int i = 0; i < n; ++i) {
-      const int32_t pg_next = tile_page(i + 1);
-      if (!store(i, v)) break;
-      if (i + 1 < n) load(i + 1, pg_next, v);
+    if (kFp8) {
+      const uint8_t* raw = sh.raw + ct * 16;
+      const uint32_t raw_s = smem_u32(raw);
+      if (n > 0) {
+        issue(0, tile_page(0), raw_s);
+        fetch(raw, v);
+      }
+      if (n > 1) issue(1, tile_page(1), raw_s);
+      for (int i = 0; i < n; ++i) {
+        const int32_t pg2 = tile_page(i + 2);
+        if (!store(i, v)) break;
+        if (i + 1 < n) {
+          fetch(raw, v);
+          if (i + 2 < n) issue(i + 2, pg2, raw_s);
+        }
+      }
+      cp_async_wait_all();  // nothing may land in shared memory after the CTA exits
+    } else {
+      if (n > 0) load(0, tile_page(0), v);
+      for (int i = 0; i < n; ++i) {
+        const int32_t pg_next = tile_page(i + 1);
+        if (!store(i, v)) break;
+        if (i + 1 < n) load(i + 1, pg_next, v);
+      }
     }
     if (bad_page) raise_status(p.status, DCP_STATUS_BAD_PAGE);
   }
@@ -811,8 +862,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (cta == 0) run_softmax<kFp8, 4>(p, sh, it, tbase, tid, warp);
     else run_softmax<kFp8, 5>(p, sh, it, tbase, tid, warp);
   } else if (warp < kMmaWarpS) {
-    if (cta == 0) Producer<kFp8, 4>(p, sh, it, tid - kProdWarp0 * 32).run();
-    else Producer<kFp8, 5>(p, sh, it, tid - kProdWarp0 * 32).run();
+    const int ct = tid - kProdWarp0 * 32;
+    if (cta == 0) Producer<kFp8, 4>(p, sh, it, ct).run(ct);
+    else Producer<kFp8, 5>(p, sh, it, ct).run(ct);
   } else if (warp == kMmaWarpS) {
     if (cta == 0) run_score_chain<kFp8, 4>(p, sh, it, tbase);
     else run_score_chain<kFp8, 5>(p, sh, it, tbase);
