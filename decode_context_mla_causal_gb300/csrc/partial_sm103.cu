@@ -680,8 +680,14 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
       for (int c = 4; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], e_cur[c]);
       const float m_cur = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sc;  // -inf: none visible
       const float bias = m_cur == -INFINITY ? 0.f : kFactorLog2 - m_cur;
+      // x*sc + bias two at a time (packed fp32 FMA), then 2^. on the MUFU unit
+      const float2 sc2 = make_float2(sc, sc), bias2 = make_float2(bias, bias);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) e_cur[c] = fast_exp2(fmaf(e_cur[c], sc, bias));
+      for (int c = 0; c < 32; c += 2) {
+        const float2 y = __ffma2_rn(make_float2(e_cur[c], e_cur[c + 1]), sc2, bias2);
+        e_cur[c] = fast_exp2(y.x);
+        e_cur[c + 1] = fast_exp2(y.y);
+      }
       // own half maximum for the partner warp (same rows, other half)
       sh.mown[((i % kMOwnBufs) * 2 + h) * kRows + r] = m_cur;
       __syncwarp();
@@ -748,7 +754,8 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
       // p = E_own * E_peer * 2^(m_own + m_peer - M); both factors carry 2^14. 8 tokens per
       // (rolled) step, read from the peer's slot and this thread's own-factor buffer
       const float f = ub_h == -INFINITY ? 0.f : fast_exp2(ub_h - M - 2.0f * kFactorLog2);
-      float lsum = 0.f;
+      const float2 f2 = make_float2(f, f);
+      float2 lsum2 = make_float2(0.f, 0.f);
       const uint4* pe_src = reinterpret_cast<const uint4*>(src) + h * 4 * kRows + r;
 #pragma unroll 1
       for (int g = 0; g < 4; ++g) {
@@ -760,16 +767,16 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
+          // two weights at a time (packed fp32): p = (E_own * f) * E_peer
           const float2 ep = __half22float2(*reinterpret_cast<const __half2*>(&pw[e]));
-          const float p0 = ow[2 * e] * f * ep.x;
-          const float p1 = ow[2 * e + 1] * f * ep.y;
+          const float2 pp = __fmul2_rn(__fmul2_rn(make_float2(ow[2 * e], ow[2 * e + 1]), f2), ep);
           // l sums the fp32 weights; the P.V contraction uses P rounded to 16 bits
-          lsum += p0 + p1;
+          lsum2 = __fadd2_rn(lsum2, pp);
           if (kFp8) {
-            __half2 hh = __floats2half2_rn(p0, p1);
+            __half2 hh = __floats2half2_rn(pp.x, pp.y);
             pk[e] = *reinterpret_cast<uint32_t*>(&hh);
           } else {
-            __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+            __nv_bfloat162 hh = __floats2bfloat162_rn(pp.x, pp.y);
             pk[e] = *reinterpret_cast<uint32_t*>(&hh);
           }
         }
@@ -778,7 +785,7 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
       __syncwarp();
       // done with the peer's slot: its values are in registers already
       if (lane == 0) mbar_arrive_remote_relaxed(xfree_remote + 8 * slot);
-      l_half += lsum;
+      l_half += lsum2.x + lsum2.y;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
