@@ -249,10 +249,15 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// E4M3 x2 -> f16 x2 (exact): the hardware conversion.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_bytes & 0xFFFFu), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Four E4M3 codes -> two f16x2 words (exact): the hardware conversion applied to
+// both 16-bit halves of the word (byte k of x becomes half k of the result).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
 }
 
 // ----------------------------------------------------------------- producers
@@ -372,14 +377,10 @@ struct Producer {
         const uint4 x = v[a * kToks + j];
         if (kFp8) {
           uint4 lo, hi;
-          lo.x = e4m3x2_to_f16x2(x.x);
-          lo.y = e4m3x2_to_f16x2(x.x >> 16);
-          lo.z = e4m3x2_to_f16x2(x.y);
-          lo.w = e4m3x2_to_f16x2(x.y >> 16);
-          hi.x = e4m3x2_to_f16x2(x.z);
-          hi.y = e4m3x2_to_f16x2(x.z >> 16);
-          hi.z = e4m3x2_to_f16x2(x.w);
-          hi.w = e4m3x2_to_f16x2(x.w >> 16);
+          e4m3x4_to_f16x4(x.x, lo.x, lo.y);
+          e4m3x4_to_f16x4(x.y, lo.z, lo.w);
+          e4m3x4_to_f16x4(x.z, hi.x, hi.y);
+          e4m3x4_to_f16x4(x.w, hi.z, hi.w);
           *reinterpret_cast<uint4*>(dst) = lo;
           // chunk 2q+1 = (2q ^ (tk & 7)) ^ 1 within the row: 16 bytes further or back
           *reinterpret_cast<uint4*>(reinterpret_cast<uintptr_t>(dst) ^ 16u) = hi;
@@ -453,13 +454,16 @@ __device__ __forceinline__ void run_score_chain(const Params& p, const Shared& s
         break;
       tc_fence_after();
       const uint64_t bdesc0 = smem_desc_sw128(stage0 + st * kStageBytes, 16, 1024);
+      if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < 4 * kAtoms; ++kk)
-        mma_f16_ts_elect(tbase + kColS, tbase + kColQ + 8 * kk,
-                         bdesc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idq,
-                         kk > 0 ? 1u : 0u);
-      tc_commit_elect(&sh.bars[kBarSFull]);
-      tc_commit_elect(&sh.bars[kBarKvEmpty + st]);
+        for (int kk = 0; kk < 4 * kAtoms; ++kk)
+          mma_f16_ts(tbase + kColS, tbase + kColQ + 8 * kk,
+                     bdesc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idq,
+                     kk > 0 ? 1u : 0u);
+        tc_commit(&sh.bars[kBarSFull]);
+        tc_commit(&sh.bars[kBarKvEmpty + st]);
+      }
+      __syncwarp();
     }
   }
   // drain: every MMA issued above has completed before TMEM can be released
@@ -480,12 +484,15 @@ __device__ __forceinline__ void run_pv(const Params& p, const Shared& sh, const 
     const uint64_t vdesc0 = smem_desc_sw128(stage0 + (j % kStages) * kStageBytes, kAtomBytes, 1024);
     const uint32_t tp = tbase + kColP;
     const uint32_t acc0 = j > 0 ? 1u : 0u;
+    if (elect_one()) {
 #pragma unroll
-    for (int kk = 0; kk < kTileN / 16; ++kk)
-      mma_f16_ts_elect(tbase + kColO, tp + 8 * kk, vdesc0 + (uint64_t)((kk * 2048) >> 4), idp,
-                       kk > 0 ? 1u : acc0);
-    tc_commit_elect(&sh.bars[kBarODone]);
-    tc_commit_elect(&sh.bars[kBarKvEmpty + (j % kStages)]);
+      for (int kk = 0; kk < kTileN / 16; ++kk)
+        mma_f16_ts(tbase + kColO, tp + 8 * kk, vdesc0 + (uint64_t)((kk * 2048) >> 4), idp,
+                   kk > 0 ? 1u : acc0);
+      tc_commit(&sh.bars[kBarODone]);
+      tc_commit(&sh.bars[kBarKvEmpty + (j % kStages)]);
+    }
+    __syncwarp();
   }
   tc_commit_elect(&sh.bars[kBarDrainP]);
   int never = 0;
