@@ -402,20 +402,15 @@ struct Producer {
     const int n = it.n_tiles;
     uint4 v[kLoads];
     if (kFp8) {
+      // step j: store tile j-1 (registers), fetch tile j (staging -> registers),
+      // issue tile j+1 (global -> staging); one code site each
       const uint8_t* raw = sh.raw + ct * 16;
       const uint32_t raw_s = smem_u32(raw);
-      if (n > 0) {
-        issue(0, tile_page(0), raw_s);
-        fetch(raw, v);
-      }
-      if (n > 1) issue(1, tile_page(1), raw_s);
-      for (int i = 0; i < n; ++i) {
-        const int32_t pg2 = tile_page(i + 2);
-        if (!store(i, v)) break;
-        if (i + 1 < n) {
-          fetch(raw, v);
-          if (i + 2 < n) issue(i + 2, pg2, raw_s);
-        }
+      for (int j = -1; j <= n; ++j) {
+        const int32_t pg = tile_page(j + 1);
+        if (j >= 1 && !store(j - 1, v)) break;
+        if (j >= 0 && j < n) fetch(raw, v);
+        if (j + 1 < n) issue(j + 1, pg, raw_s);
       }
       cp_async_wait_all();  // nothing may land in shared memory after the CTA exits
     } else {
