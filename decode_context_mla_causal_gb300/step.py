@@ -26,9 +26,12 @@ def choose_num_splits(batch: int, qlen: int, num_heads: int, num_ranks: int,
 
     Each work item (rank, sequence, split, 128-row tile) runs on a cluster of two
     CTAs, one CTA per SM, so ``sms // 2`` items run at once. The cost model is
-    waves * (64-token tiles per split + 2 tiles of per-item overhead), evaluated
-    at the static bound; the cheapest split count wins (ties: fewer splits).
-    Uses only static sizes, so the choice is graph-safe.
+    waves * (64-token tiles per split + 11 tiles of per-item overhead) + 0.5 tile
+    per split for the merge's extra partial rows, evaluated at the static bound;
+    the per-item overhead (start-up, pipeline fill, epilogue) was fitted to
+    measured times over split counts 10-20 of the long-context workload. The
+    cheapest split count wins (ties: fewer splits). Uses only static sizes, so the
+    choice is graph-safe.
     """
     tiles = max(1, math.ceil(max_local_len / 64))
     row_tiles = math.ceil(qlen * num_heads / 128)
@@ -36,7 +39,7 @@ def choose_num_splits(batch: int, qlen: int, num_heads: int, num_ranks: int,
     slots = max(1, sms // 2)
     best = None
     for ns in range(1, min(64, tiles) + 1):
-        cost = math.ceil(base * ns / slots) * (tiles / ns + 2.0)
+        cost = math.ceil(base * ns / slots) * (tiles / ns + 11.0) + 0.5 * ns
         if best is None or cost < best[0] - 1e-9:
             best = (cost, ns)
     return int(best[1])
