@@ -535,20 +535,28 @@ __device__ __noinline__ void store_o(uint32_t tO, bool have_o, bool row_ok, floa
 }
 
 // Q slice of one row into TMEM (16-bit, 2 per column; atom a at columns 32a);
-// half 0 loads atoms 0-2, half 1 the rest. Returns true if some |q| exceeds the
-// f16 range on the FP8 path.
+// half 0 loads atoms 0-2, half 1 the rest. The next atom's 128 bytes are
+// requested before the current one is converted, so the global latency is paid
+// about once. Returns true if some |q| exceeds the f16 range on the FP8 path.
 template <bool kFp8, int kAtoms>
 __device__ __noinline__ bool load_q(const uint16_t* src, bool row_ok, int h, uint32_t tQ) {
   bool q_range = false;
   const int a0 = h == 0 ? 0 : 3;
   const int a1 = h == 0 ? 3 : kAtoms;
+  uint4 cur[8], nxt[8];
+  auto fetch = [&](int a, uint4 (&v)[8]) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      v[c] = (row_ok && a < a1) ? __ldg(reinterpret_cast<const uint4*>(src + a * 64 + c * 8))
+                                : make_uint4(0u, 0u, 0u, 0u);
+  };
+  fetch(a0, cur);
   for (int a = a0; a < a1; ++a) {
+    fetch(a + 1, nxt);
     uint32_t w[32];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (row_ok) v = __ldg(reinterpret_cast<const uint4*>(src + a * 64 + c * 8));
-      const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+      const uint32_t x[4] = {cur[c].x, cur[c].y, cur[c].z, cur[c].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         if (kFp8) {
@@ -563,6 +571,8 @@ __device__ __noinline__ bool load_q(const uint16_t* src, bool row_ok, int h, uin
       }
     }
     tmem_st32(tQ + 32 * a, w);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) cur[c] = nxt[c];
   }
   tmem_wait_st();
   return q_range;
