@@ -764,12 +764,13 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
       tc_fence_after();
       if (t >= 1 && __any_sync(0xffffffffu, need)) rescale_o(tO, need ? alpha : 1.f);
       // p = E_own * E_peer * 2^(m_own + m_peer - M); both factors carry 2^14. 8 tokens per
-      // (rolled) step, read from the peer's slot and this thread's own-factor buffer
+      // step (two steps per loop body), read from the peer's slot and this thread's
+      // own-factor buffer
       const float f = ub_h == -INFINITY ? 0.f : fast_exp2(ub_h - M - 2.0f * kFactorLog2);
       const float2 f2 = make_float2(f, f);
       float2 lsum2 = make_float2(0.f, 0.f);
       const uint4* pe_src = reinterpret_cast<const uint4*>(src) + h * 4 * kRows + r;
-#pragma unroll 1
+#pragma unroll 2
       for (int g = 0; g < 4; ++g) {
         const uint4 pe = pe_src[g * kRows];
         const float4 own0 = eprev[(2 * g) * kRows];
