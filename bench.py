@@ -316,6 +316,29 @@ def main():
         dist.all_reduce(te, op=dist.ReduceOp.MAX)
     e2e_value = tokens * world * K / (float(te.item()) / 1e3)
 
+    # the step before the path: the new tokens' slot mapping and KV write (FP8:
+    # quantisation), timed on its own after the verify step (it overwrites the
+    # new tokens' cache rows with synthetic values)
+    new_rows = torch.randn((w.rows, 576), generator=torch.Generator(device=dev).manual_seed(17),
+                           device=dev).to(torch.bfloat16)
+    slots = torch.empty((w.dcp, w.rows), dtype=torch.int32, device=dev)
+    kv_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kw_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for i in range(args.warmup + K):
+        if i >= args.warmup:
+            kw_ev[i - args.warmup][0].record(stream)
+        dm.dcp_kv_slot_mapping(dims, w.seq_lens, w.block_table, 0, w.dcp, slots, kv_status)
+        if i >= args.warmup:
+            kw_ev[i - args.warmup][1].record(stream)
+        dm.dcp_kv_write(dims, slots, new_rows, kvt, scale, w.dcp, w.kv, kv_status)
+        if i >= args.warmup:
+            kw_ev[i - args.warmup][2].record(stream)
+    torch.cuda.synchronize()
+    if int(kv_status.item()) != 0:
+        raise RuntimeError(f"kv write status {int(kv_status.item()):#x}")
+    kv_map_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in kw_ev) / K
+    kv_write_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in kw_ev) / K
+
     peaks, src = load_peaks()
     part_avg = sum(part_ms) / K
     achieved_tf = flops / (part_avg / 1e3) / 1e12
@@ -350,6 +373,10 @@ def main():
                      "hbm_frac_of_partial": nbytes / (part_avg / 1e3) / (hbm_peak * 1e9)},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
+        "kv_write": {"kernel_us": {"slot_mapping": kv_map_us, "write": kv_write_us},
+                     "rows": w.rows, "ranks": w.dcp,
+                     "note": "new-token KV write (the step before the verify path), timed "
+                             "separately; not part of ms_per_step"},
         "gpu_launches": 3 * K,
         "clocks": clocks,
     }

@@ -85,6 +85,8 @@ def load() -> ctypes.CDLL:
         "dcp_mla_partial": (I, [D, P, P, I, P, ctypes.c_float, I, I, P, P, P, P, P, P, P, P, P]),
         "dcp_lse_merge": (I, [D, I, P, P, P, P, P, P, P, P]),
         "dcp_mla_verify_noalloc": (I, [D, P, P, P, P, I, P, ctypes.c_float, P, P, P, P]),
+        "dcp_kv_slot_mapping": (I, [D, P, P, I, I, P, P, P]),
+        "dcp_kv_write": (I, [D, P, P, I, P, I, P, P, P]),
         "dcp_last_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -200,6 +202,32 @@ def dcp_lse_merge(dims, num_ranks, part_o, part_m, part_l, out, lse, rank_lse=No
         _ptr(out, torch.bfloat16, R * H * V_DIM, "out"),
         _ptr(lse, f32, R * H, "lse"),
         _ptr(rank_lse, f32, num_ranks * R * H, "rank_lse", allow_none=True),
+        _ptr(status, torch.int32, 1, "status"), _stream(stream)))
+
+
+def dcp_kv_slot_mapping(dims, seq_lens, block_table, rank_begin, num_ranks, slot_mapping,
+                        status, stream=None):
+    """Pool row of each new token on each rank (-1 where the rank does not own it)."""
+    lib = load()
+    i32 = torch.int32
+    _check(lib.dcp_kv_slot_mapping(
+        ctypes.byref(dims), _ptr(seq_lens, i32, dims.batch, "seq_lens"),
+        _ptr(block_table, i32, dims.batch * dims.max_blocks_per_seq, "block_table"),
+        int(rank_begin), int(num_ranks),
+        _ptr(slot_mapping, i32, num_ranks * dims.rows, "slot_mapping"),
+        _ptr(status, i32, 1, "status"), _stream(stream)))
+
+
+def dcp_kv_write(dims, slot_mapping, kv_new, kv_dtype, kv_scale, num_ranks, pool, status,
+                 stream=None):
+    """Writes (FP8: quantises) the new tokens' rows into the rank pools."""
+    lib = load()
+    kv_elem = torch.uint8 if kv_dtype == KV_FP8_E4M3 else torch.bfloat16
+    _check(lib.dcp_kv_write(
+        ctypes.byref(dims), _ptr(slot_mapping, torch.int32, num_ranks * dims.rows, "slot_mapping"),
+        _ptr(kv_new, torch.bfloat16, dims.rows * QK_DIM, "kv_new"), int(kv_dtype),
+        _ptr(kv_scale, torch.float32, 1, "kv_scale", allow_none=True), int(num_ranks),
+        _ptr(pool, kv_elem, num_ranks * dims.num_blocks * dims.block_size * QK_DIM, "pool"),
         _ptr(status, torch.int32, 1, "status"), _stream(stream)))
 
 

@@ -152,6 +152,36 @@ dcp_status dcp_lse_merge(const dcp_mla_dims* dims, int32_t num_ranks, const floa
                   "dcp_lse_merge");
 }
 
+dcp_status dcp_kv_slot_mapping(const dcp_mla_dims* dims, const int32_t* seq_lens,
+                               const int32_t* block_table, int32_t rank_begin, int32_t num_ranks,
+                               int32_t* slot_mapping, uint32_t* status, dcp_stream_t stream) {
+  dcp_status s = check(dims, rank_begin, num_ranks);
+  if (s != DCP_OK) return s;
+  if (dims->batch == 0 || num_ranks == 0) return DCP_OK;
+  if (!seq_lens || !block_table || !slot_mapping || !status)
+    return fail(DCP_ERR_INVALID_ARG, "dcp_kv_slot_mapping: a required pointer is NULL");
+  return launched(launch_slot_mapping(*dims, seq_lens, block_table, rank_begin, num_ranks,
+                                      slot_mapping, status, (cudaStream_t)stream),
+                  "dcp_kv_slot_mapping");
+}
+
+dcp_status dcp_kv_write(const dcp_mla_dims* dims, const int32_t* slot_mapping, const void* kv_new,
+                        dcp_kv_dtype kv_dtype, const float* kv_scale, int32_t num_ranks,
+                        void* pool, uint32_t* status, dcp_stream_t stream) {
+  dcp_status s = check(dims, 0, num_ranks);
+  if (s != DCP_OK) return s;
+  if (kv_dtype != DCP_KV_BF16 && kv_dtype != DCP_KV_FP8_E4M3)
+    return fail(DCP_ERR_INVALID_ARG, "unknown kv_dtype %d", (int)kv_dtype);
+  if (dims->batch == 0 || num_ranks == 0) return DCP_OK;
+  if (!slot_mapping || !kv_new || !pool || !status)
+    return fail(DCP_ERR_INVALID_ARG, "dcp_kv_write: a required pointer is NULL");
+  if (((uintptr_t)kv_new & 15) || ((uintptr_t)pool & 15))
+    return fail(DCP_ERR_INVALID_ARG, "kv_new and pool must be 16-byte aligned");
+  return launched(launch_kv_write(*dims, slot_mapping, kv_new, kv_dtype, kv_scale, num_ranks,
+                                  pool, status, (cudaStream_t)stream),
+                  "dcp_kv_write");
+}
+
 const char* dcp_last_error(void) { return g_last_error.c_str(); }
 
 }  // extern "C"

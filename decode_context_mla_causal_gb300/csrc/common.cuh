@@ -42,6 +42,14 @@ cudaError_t launch_merge(const dcp_mla_dims& d, const Derived& x, int num_ranks,
                          void* out, float* lse, float* rank_lse, uint32_t* status,
                          cudaStream_t stream);
 
+cudaError_t launch_slot_mapping(const dcp_mla_dims& d, const int32_t* seq_lens,
+                                const int32_t* block_table, int rank_begin, int num_ranks,
+                                int32_t* slot_mapping, uint32_t* status, cudaStream_t stream);
+
+cudaError_t launch_kv_write(const dcp_mla_dims& d, const int32_t* slot_mapping, const void* kv_new,
+                            dcp_kv_dtype kv_dtype, const float* kv_scale, int num_ranks,
+                            void* pool, uint32_t* status, cudaStream_t stream);
+
 __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bits) {
   if (status != nullptr) atomicOr(status, bits);
 }

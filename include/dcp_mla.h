@@ -223,6 +223,47 @@ dcp_status dcp_mla_verify_noalloc(const dcp_mla_dims* dims, const int32_t* seq_l
                                   float softmax_scale, void* out, float* lse, uint32_t* status,
                                   dcp_stream_t stream);
 
+/*
+ * The step before the path: writing the new (verify) tokens' latent KV rows
+ * into the interleaved rank pools.
+ * Defined by: "Context Parallel Guide (PCP & DCP)", "How it works" 2 (new-token
+ * KV is written interleaved via slot_mapping, -1 for tokens a rank does not own)
+ * and 4 (FP8 cache with one per-tensor scale); "Support Kimi-K3 DCP with DSpark"
+ * (the owning rank of global position p and the slot on that rank), with the
+ * interleave of the "--dcp-config" table.
+ *
+ * dcp_kv_slot_mapping:
+ *   seq_lens     device int32 [B]      global lengths incl. the qlen new tokens;
+ *                                      new token j of sequence b is at global
+ *                                      position seq_lens[b] - qlen + j
+ *   block_table  device int32 [B][MB]  shared block ids
+ *   slot_mapping device int32 [nr][R]  out: pool row (block*block_size + offset)
+ *                                      of token row b*qlen+j in the pool of rank
+ *                                      rank_begin+k, or -1 where that rank does
+ *                                      not own the token or the slot is invalid
+ *   status       device uint32 [1]     in/out: DCP_STATUS_BAD_SEQ_LEN (seq_len <
+ *                                      qlen), DCP_STATUS_LOCAL_OVER_BOUND (local
+ *                                      index >= MB*block_size),
+ *                                      DCP_STATUS_BAD_BLOCK_ID (id outside [0, NB))
+ * dcp_kv_write:
+ *   slot_mapping device int32 [nr][R]  dcp_kv_slot_mapping's output
+ *   kv_new       device bf16 [R][576]  the new tokens' latent rows (row b*qlen+j)
+ *   kv_scale     device float [1]      FP8 pools: code = E4M3(x / kv_scale) with
+ *                                      x / kv_scale an IEEE fp32 division, rounded
+ *                                      to nearest even, saturated to +-448 (NULL =
+ *                                      1); ignored for BF16 pools (bits copied)
+ *   pool         device [nr][NB][block_size][576] E4M3 codes or bf16: the rows
+ *                named by slot_mapping are overwritten, nothing else is touched
+ * Entries of slot_mapping outside [-1, NB*block_size) set DCP_STATUS_BAD_PAGE and
+ * are skipped.
+ */
+dcp_status dcp_kv_slot_mapping(const dcp_mla_dims* dims, const int32_t* seq_lens,
+                               const int32_t* block_table, int32_t rank_begin, int32_t num_ranks,
+                               int32_t* slot_mapping, uint32_t* status, dcp_stream_t stream);
+dcp_status dcp_kv_write(const dcp_mla_dims* dims, const int32_t* slot_mapping, const void* kv_new,
+                        dcp_kv_dtype kv_dtype, const float* kv_scale, int32_t num_ranks,
+                        void* pool, uint32_t* status, dcp_stream_t stream);
+
 /* Message for the last non-OK return on this thread ("" if none). */
 const char* dcp_last_error(void);
 

@@ -15,6 +15,10 @@ Everything is plain NumPy in float64 and follows the plain definitions:
 * ``attention``  -- gather of a global sequence from the interleaved rank
                     pools, global causal attention, per-shard attention and the
                     LSE merge of shard results.
+* ``kv_write``   -- the step before the path: the new tokens' slot mapping
+                    (-1 where a rank does not own a token), the E4M3 encoding of
+                    x / scale (round to nearest even, saturating) and the write
+                    into the rank pools.
 
 Sources (cited by page title and section throughout):
 
