@@ -19,6 +19,11 @@ Everything is plain NumPy in float64 and follows the plain definitions:
                     (-1 where a rank does not own a token), the E4M3 encoding of
                     x / scale (round to nearest even, saturating) and the write
                     into the rank pools.
+* ``exchange``   -- the step after the path: each rank's output in the
+                    all-to-all wire format (BF16 output, the float32 LSE as two
+                    16-bit halves), the all-to-all itself, the combine at the
+                    destination, and project-before-merge (a per-head W_V
+                    applied to each rank's output before the exchange).
 
 Sources (cited by page title and section throughout):
 
@@ -30,9 +35,9 @@ Sources (cited by page title and section throughout):
 * "[ROCm][MLA][DCP] Support causal multi-token verification" (vLLM PR #51705),
   sections "Implementation" and "Validation": the verify path itself.
 
-Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
-except the split/partial intermediates, which are implementation-defined and
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``,
+``tests/test_kv_write_pins.py`` or ``tests/test_exchange_pins.py`` except the split/partial intermediates, which are implementation-defined and
 therefore never compared (only merged outputs and per-rank LSE are).
 """
 
-from . import fp8, metadata, attention  # noqa: F401
+from . import fp8, metadata, attention, kv_write, exchange  # noqa: F401
