@@ -339,6 +339,46 @@ def main():
     kv_map_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in kw_ev) / K
     kv_write_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in kw_ev) / K
 
+    # the step after the path: each rank's result in the all-to-all wire format
+    # (pack), then the combine with every rank on this device; plain (512 latent
+    # dims per head) and with project-before-merge (synthetic W_V, 512 -> 128)
+    a2a = None
+    if w.num_heads % w.dcp == 0:
+        a2a = {}
+        w_v = workloads.generate_w_v(w.num_heads, 128, device=dev)
+        nr, R, H = w.dcp, w.rows, w.num_heads
+        for label, wv in (("plain", None), ("project_before_merge", w_v)):
+            ex = dm.A2AExchange(step, w_v=wv)
+            a_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+            for i in range(args.warmup + K):
+                if i >= args.warmup:
+                    a_ev[i - args.warmup][0].record(stream)
+                ex.pack(stream)
+                if i >= args.warmup:
+                    a_ev[i - args.warmup][1].record(stream)
+                ex.combine_local(stream)
+                if i >= args.warmup:
+                    a_ev[i - args.warmup][2].record(stream)
+            torch.cuda.synchronize()
+            if step.read_status() != 0:
+                raise RuntimeError(f"a2a status {step.read_status():#x}")
+            pack_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in a_ev) / K
+            comb_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in a_ev) / K
+            send_bytes = ex.send.numel() * 2
+            pack_bytes = nr * ns * R * H * (4 * 512 + 8) + send_bytes
+            comb_bytes = send_bytes + R * H * (2 * ex.payload + 4)
+            a2a[label] = {"payload": ex.payload, "send_bytes": send_bytes,
+                          "kernel_us": {"pack": pack_us, "combine": comb_us},
+                          "pack_hbm_gbs": pack_bytes / (pack_us / 1e6) / 1e9,
+                          "combine_hbm_gbs": comb_bytes / (comb_us / 1e6) / 1e9}
+            if wv is not None:
+                a2a[label]["pack_projection_tflops"] = (
+                    2.0 * nr * R * H * 512 * ex.payload / (pack_us / 1e6) / 1e12)
+            del ex
+        a2a["note"] = ("all-to-all wire format (BF16 output + float32 LSE as two 16-bit "
+                       "halves), combined on this device; timed separately, not part of "
+                       "ms_per_step")
+
     peaks, src = load_peaks()
     part_avg = sum(part_ms) / K
     achieved_tf = flops / (part_avg / 1e3) / 1e12
@@ -377,6 +417,7 @@ def main():
                      "rows": w.rows, "ranks": w.dcp,
                      "note": "new-token KV write (the step before the verify path), timed "
                              "separately; not part of ms_per_step"},
+        "a2a": a2a,
         "gpu_launches": 3 * K,
         "clocks": clocks,
     }

@@ -87,6 +87,9 @@ def load() -> ctypes.CDLL:
         "dcp_mla_verify_noalloc": (I, [D, P, P, P, P, I, P, ctypes.c_float, P, P, P, P]),
         "dcp_kv_slot_mapping": (I, [D, P, P, I, I, P, P, P]),
         "dcp_kv_write": (I, [D, P, P, I, P, I, P, P, P]),
+        "dcp_a2a_chunk_words": (ctypes.c_int64, [D, I]),
+        "dcp_a2a_pack": (I, [D, I, P, P, P, P, I, P, P, P]),
+        "dcp_a2a_combine": (I, [D, I, P, ctypes.c_int64, ctypes.c_int64, I, I, P, P, P, P]),
         "dcp_last_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -229,6 +232,47 @@ def dcp_kv_write(dims, slot_mapping, kv_new, kv_dtype, kv_scale, num_ranks, pool
         _ptr(kv_scale, torch.float32, 1, "kv_scale", allow_none=True), int(num_ranks),
         _ptr(pool, kv_elem, num_ranks * dims.num_blocks * dims.block_size * QK_DIM, "pool"),
         _ptr(status, torch.int32, 1, "status"), _stream(stream)))
+
+
+def dcp_a2a_chunk_words(dims, payload=V_DIM) -> int:
+    """16-bit words of one (source, destination) chunk of the all-to-all wire format."""
+    n = load().dcp_a2a_chunk_words(ctypes.byref(dims), int(payload))
+    if n < 0:
+        raise DcpError(DCP_ERR_INVALID_ARG, "invalid dims or payload for the wire format")
+    return int(n)
+
+
+def dcp_a2a_pack(dims, num_ranks, part_o, part_m, part_l, send, w_v=None, payload=V_DIM,
+                 status=None, stream=None):
+    """Each rank's merged output and LSE in the all-to-all wire format (``send`` is a
+    bf16 tensor of ``num_ranks * dcp * chunk_words`` elements); with ``w_v`` (bf16
+    ``[H][payload][512]``) the output is projected first (project-before-merge)."""
+    lib = load()
+    R, H = dims.rows, dims.num_heads
+    parts = num_ranks * dims.num_splits * R * H
+    cw = dcp_a2a_chunk_words(dims, payload)
+    _check(lib.dcp_a2a_pack(
+        ctypes.byref(dims), int(num_ranks), _ptr(part_o, torch.float32, parts * V_DIM, "part_o"),
+        _ptr(part_m, torch.float32, parts, "part_m"), _ptr(part_l, torch.float32, parts, "part_l"),
+        _ptr(w_v, torch.bfloat16, H * payload * V_DIM, "w_v", allow_none=True), int(payload),
+        _ptr(send, torch.bfloat16, num_ranks * dims.dcp * cw, "send"),
+        _ptr(status, torch.int32, 1, "status", allow_none=True), _stream(stream)))
+
+
+def dcp_a2a_combine(dims, payload, recv, src_stride, dst_stride, dst_begin, num_dst, out, lse,
+                    status=None, stream=None):
+    """Combine at destination ranks ``dst_begin .. dst_begin+num_dst-1`` of the chunks
+    they received (strides in 16-bit words); writes their heads of ``out`` (bf16
+    ``[R][H][payload]``) and ``lse`` (float ``[R][H]``)."""
+    lib = load()
+    R, H = dims.rows, dims.num_heads
+    cw = dcp_a2a_chunk_words(dims, payload)
+    need = (num_dst - 1) * dst_stride + (dims.dcp - 1) * src_stride + cw
+    _check(lib.dcp_a2a_combine(
+        ctypes.byref(dims), int(payload), _ptr(recv, torch.bfloat16, need, "recv"),
+        int(src_stride), int(dst_stride), int(dst_begin), int(num_dst),
+        _ptr(out, torch.bfloat16, R * H * payload, "out"), _ptr(lse, torch.float32, R * H, "lse"),
+        _ptr(status, torch.int32, 1, "status", allow_none=True), _stream(stream)))
 
 
 def dcp_mla_verify_noalloc(dims, seq_lens, block_table, q, kv, kv_dtype, kv_scale,

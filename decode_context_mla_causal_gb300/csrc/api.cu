@@ -182,6 +182,64 @@ dcp_status dcp_kv_write(const dcp_mla_dims* dims, const int32_t* slot_mapping, c
                   "dcp_kv_write");
 }
 
+int64_t dcp_a2a_chunk_words(const dcp_mla_dims* dims, int32_t payload) {
+  if (check(dims, 0, 1) != DCP_OK) return -1;
+  if (payload < 1 || payload > kDv || dims->num_heads % dims->dcp != 0) return -1;
+  return dcpmla::a2a_chunk_words(dims->batch * dims->qlen, dims->num_heads / dims->dcp, payload);
+}
+
+dcp_status dcp_a2a_pack(const dcp_mla_dims* dims, int32_t num_ranks, const float* part_o,
+                        const float* part_m, const float* part_l, const void* w_v,
+                        int32_t payload, void* send, uint32_t* status, dcp_stream_t stream) {
+  dcp_status s = check(dims, 0, num_ranks);
+  if (s != DCP_OK) return s;
+  if (dims->num_heads % dims->dcp != 0)
+    return fail(DCP_ERR_INVALID_ARG, "num_heads (%d) must be a multiple of dcp (%d)",
+                dims->num_heads, dims->dcp);
+  if (w_v == nullptr && payload != kDv)
+    return fail(DCP_ERR_INVALID_ARG, "payload must be 512 without w_v (got %d)", payload);
+  if (w_v != nullptr && (payload < 16 || payload > 256 || payload % 16 != 0))
+    return fail(DCP_ERR_INVALID_ARG, "projected payload must be a multiple of 16 in [16, 256]");
+  if (dims->batch == 0) return DCP_OK;
+  if (!part_o || !part_m || !part_l || !send)
+    return fail(DCP_ERR_INVALID_ARG, "dcp_a2a_pack: a required pointer is NULL");
+  if (((uintptr_t)part_o & 15) || ((uintptr_t)send & 15) || ((uintptr_t)w_v & 15))
+    return fail(DCP_ERR_INVALID_ARG, "part_o, send and w_v must be 16-byte aligned");
+  Derived x = derive(*dims);
+  if (w_v == nullptr)
+    return launched(launch_a2a_pack(*dims, x, num_ranks, part_o, part_m, part_l, send,
+                                    (cudaStream_t)stream),
+                    "dcp_a2a_pack");
+  return launched(launch_a2a_pack_projected(*dims, x, num_ranks, part_o, part_m, part_l, w_v,
+                                            payload, send, status, (cudaStream_t)stream),
+                  "dcp_a2a_pack");
+}
+
+dcp_status dcp_a2a_combine(const dcp_mla_dims* dims, int32_t payload, const void* recv,
+                           int64_t src_stride, int64_t dst_stride, int32_t dst_begin,
+                           int32_t num_dst, void* out, float* lse, uint32_t* status,
+                           dcp_stream_t stream) {
+  (void)status;
+  dcp_status s = check(dims, dst_begin, num_dst);
+  if (s != DCP_OK) return s;
+  if (dims->num_heads % dims->dcp != 0)
+    return fail(DCP_ERR_INVALID_ARG, "num_heads (%d) must be a multiple of dcp (%d)",
+                dims->num_heads, dims->dcp);
+  if (payload < 4 || payload > kDv || payload % 4 != 0)
+    return fail(DCP_ERR_INVALID_ARG, "payload must be a multiple of 4 in [4, 512]");
+  if (src_stride < 0 || dst_stride < 0 || (src_stride & 7) || (dst_stride & 7))
+    return fail(DCP_ERR_INVALID_ARG, "strides must be non-negative multiples of 8 words");
+  if (dims->batch == 0) return DCP_OK;
+  if (!recv || !out || !lse)
+    return fail(DCP_ERR_INVALID_ARG, "dcp_a2a_combine: a required pointer is NULL");
+  if (((uintptr_t)recv & 15) || ((uintptr_t)out & 7))
+    return fail(DCP_ERR_INVALID_ARG, "recv must be 16-byte and out 8-byte aligned");
+  Derived x = derive(*dims);
+  return launched(launch_a2a_combine(*dims, x, payload, recv, src_stride, dst_stride, dst_begin,
+                                     num_dst, out, lse, (cudaStream_t)stream),
+                  "dcp_a2a_combine");
+}
+
 const char* dcp_last_error(void) { return g_last_error.c_str(); }
 
 }  // extern "C"

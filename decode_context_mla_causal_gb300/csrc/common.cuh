@@ -50,6 +50,22 @@ cudaError_t launch_kv_write(const dcp_mla_dims& d, const int32_t* slot_mapping, 
                             dcp_kv_dtype kv_dtype, const float* kv_scale, int num_ranks,
                             void* pool, uint32_t* status, cudaStream_t stream);
 
+int64_t a2a_chunk_words(int R, int Hg, int P);
+
+cudaError_t launch_a2a_pack(const dcp_mla_dims& d, const Derived& x, int num_ranks,
+                            const float* part_o, const float* part_m, const float* part_l,
+                            void* send, cudaStream_t stream);
+
+cudaError_t launch_a2a_pack_projected(const dcp_mla_dims& d, const Derived& x, int num_ranks,
+                                      const float* part_o, const float* part_m,
+                                      const float* part_l, const void* w_v, int payload,
+                                      void* send, uint32_t* status, cudaStream_t stream);
+
+cudaError_t launch_a2a_combine(const dcp_mla_dims& d, const Derived& x, int payload,
+                               const void* recv, int64_t src_stride, int64_t dst_stride,
+                               int dst_begin, int num_dst, void* out, float* lse,
+                               cudaStream_t stream);
+
 __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bits) {
   if (status != nullptr) atomicOr(status, bits);
 }

@@ -1,0 +1,390 @@
+// The step after the path: the cross-rank exchange in the all-to-all wire format.
+//
+// "Context Parallel Guide (PCP & DCP)", Decode and comm_backend "a2a": every rank
+// returns its output and LSE; ONE all-to-all carries each rank's output with the
+// LSE packed alongside it, and the destination combines locally, so that every
+// rank ends with its slice of the heads. The fp32 LSE travels as two 16-bit
+// halves of the BF16 buffer (bit for bit); the output travels as BF16.
+//
+// Wire format of the chunk a source rank sends to destination d (which owns heads
+// [d*Hg, (d+1)*Hg), Hg = H / dcp): [R][Hg][P] BF16 outputs, then [R][Hg][2] LSE
+// halves (low 16 bits, then high 16 bits of the float32), then zero words up to a
+// multiple of 8 words. A source's send buffer is [dcp][chunk].
+//
+//   a2a_pack_kernel     one CTA per (row, head, rank): merges the rank's splits
+//                       (m, l, o) into its normalised output, RNE to BF16, and its
+//                       natural-log LSE, written into the chunk for the head's
+//                       destination. HBM-bound: reads NS*(2 KiB + 8 B), writes
+//                       1 KiB + 4 B per (rank, row, head).
+//   a2a_combine_kernel  one CTA per (destination, row, head of its slice): reads the
+//                       dcp source entries, LSE-weights them. HBM-bound: reads
+//                       dcp*(2P + 4) B, writes 2P + 4 B per (row, head).
+//
+// Project-before-merge ("enable_project_before_merge" on the same page): each
+// rank's output is projected by the head's W_V before it is sent, so P = the
+// projected width instead of 512.
+//
+//   a2a_pack_projected_kernel  one CTA per (head, 128 vectors), a vector being one
+//                       (rank, row): D[128][P] = A[128][512] . W_V[h]^T on the
+//                       tensor cores (tcgen05, M = 128, N = P, K = 512 in 8 chunks
+//                       of 64, fp32 accumulator in tensor memory). The A operand is
+//                       built in place: each thread merges its vector's splits for
+//                       the chunk's 64 dims, rounds to BF16 and stores the row into
+//                       the 128-byte-swizzled K-major tile; W_V rows go to the B
+//                       tile. Two stages: the stores of chunk c overlap the MMAs of
+//                       chunk c-1. The epilogue reads D back (tcgen05.ld), rounds to
+//                       BF16 and writes the wire entries and the LSE halves.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "sm103.cuh"
+
+namespace dcpmla {
+namespace {
+
+using namespace sm103;
+
+constexpr float kLn2 = 0.6931471805599453f;
+
+__global__ void __launch_bounds__(128)
+a2a_pack_kernel(int R, int H, int G, int num_splits, int64_t cw, const float* __restrict__ part_o,
+                const float* __restrict__ part_m, const float* __restrict__ part_l,
+                uint16_t* __restrict__ send) {
+  const int rows_heads = R * H;
+  const int rh = blockIdx.x;
+  const int k = blockIdx.y;  // rank within the call
+  const int row = rh / H, h = rh % H;
+  const int Hg = H / G, d = h / Hg, hl = h % Hg;
+  const int64_t p0 = (int64_t)k * num_splits * rows_heads + rh;  // split 0 of this rank
+  float M = -INFINITY;
+  for (int s = 0; s < num_splits; ++s) M = fmaxf(M, part_m[p0 + (int64_t)s * rows_heads]);
+  const int dim = threadIdx.x * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < num_splits; ++s) {
+      const int64_t i = p0 + (int64_t)s * rows_heads;
+      const float m = part_m[i];
+      const float l = part_l[i];
+      if (m == -INFINITY || !(l > 0.f)) continue;
+      const float w = exp2f(m - M) * l;
+      den += w;
+      const float4 o = *reinterpret_cast<const float4*>(part_o + i * kDv + dim);
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
+    }
+  }
+  const float inv = den > 0.f ? 1.0f / den : 0.f;
+  uint16_t* chunk = send + ((int64_t)k * G + d) * cw;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 v;
+  v.x = *reinterpret_cast<uint32_t*>(&lo);
+  v.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(chunk + ((int64_t)row * Hg + hl) * kDv + dim) = v;
+  if (threadIdx.x == 0) {
+    const float lse = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
+    const uint32_t bits = __float_as_uint(lse);
+    uint16_t* lp = chunk + (int64_t)R * Hg * kDv + ((int64_t)row * Hg + hl) * 2;
+    lp[0] = (uint16_t)(bits & 0xFFFFu);
+    lp[1] = (uint16_t)(bits >> 16);
+  }
+  if (rh == 0) {  // the zero words that end each of this rank's chunks
+    const int64_t used = (int64_t)R * Hg * (kDv + 2);
+    for (int dd = 0; dd < G; ++dd)
+      for (int64_t w = used + threadIdx.x; w < cw; w += blockDim.x)
+        send[((int64_t)k * G + dd) * cw + w] = 0;
+  }
+}
+
+__global__ void __launch_bounds__(128)
+a2a_combine_kernel(int R, int H, int G, int P, const uint16_t* __restrict__ recv,
+                   int64_t src_stride, int64_t dst_stride, int dst_begin,
+                   __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+  const int Hg = H / G;
+  const int e = blockIdx.x;  // row * Hg + hl
+  const int di = blockIdx.y;
+  const int row = e / Hg, hl = e % Hg;
+  const int h = (dst_begin + di) * Hg + hl;
+  const uint16_t* base = recv + (int64_t)di * dst_stride;
+  const int64_t lse_off = (int64_t)R * Hg * P + (int64_t)e * 2;
+  auto lse_of = [&](int s) {
+    const uint16_t* lp = base + (int64_t)s * src_stride + lse_off;
+    return __uint_as_float((uint32_t)lp[0] | ((uint32_t)lp[1] << 16));
+  };
+  float M = -INFINITY;
+  for (int s = 0; s < G; ++s) M = fmaxf(M, lse_of(s));
+  float den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int dim = threadIdx.x * 4;
+  const bool active = dim < P;
+  if (M != -INFINITY) {
+    for (int s = 0; s < G; ++s) {
+      const float ls = lse_of(s);
+      if (ls == -INFINITY) continue;
+      const float w = expf(ls - M);
+      den += w;
+      if (active) {
+        const uint2 v =
+            *reinterpret_cast<const uint2*>(base + (int64_t)s * src_stride + (int64_t)e * P + dim);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+        acc.x = fmaf(w, a.x, acc.x);
+        acc.y = fmaf(w, a.y, acc.y);
+        acc.z = fmaf(w, b.x, acc.z);
+        acc.w = fmaf(w, b.y, acc.w);
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.0f / den : 0.f;
+  if (active) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&lo);
+    v.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + ((int64_t)row * H + h) * P + dim) = v;
+  }
+  if (threadIdx.x == 0) lse[(int64_t)row * H + h] = den > 0.f ? M + logf(den) : -INFINITY;
+}
+
+constexpr int kProjVecs = 128;                  // vectors per CTA (MMA M)
+constexpr int kProjChunk = 64;                  // K dims per stage (one 128-byte swizzle atom)
+constexpr int kProjABytes = kProjVecs * 128;    // A tile of one chunk
+constexpr uint32_t kProjTmemCols = 256;         // accumulator, P <= 256
+constexpr int kProjMinSmem = 80 * 1024;         // at most two CTAs (2 x 256 columns) per SM
+constexpr uint64_t kProjTimeoutNs = 4000000000ull;
+
+__device__ bool proj_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_wait_sleep(a, parity)) {
+    if (globaltimer_ns() - t0 > kProjTimeoutNs) {
+      raise_status(status, DCP_STATUS_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(128)
+a2a_pack_projected_kernel(int R, int H, int G, int num_ranks, int num_splits, int P, int64_t cw,
+                          const float* __restrict__ part_o, const float* __restrict__ part_m,
+                          const float* __restrict__ part_l, const uint16_t* __restrict__ w_v,
+                          uint16_t* __restrict__ send, uint32_t* status) {
+  extern __shared__ unsigned char smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int stage_bytes = kProjABytes + P * 128;  // multiple of 1024 (P % 16 == 0)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + 2 * stage_bytes);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+  const int tid = threadIdx.x;
+  const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
+  const int lane = tid & 31;
+  const int h = blockIdx.x;
+  const int Hg = H / G, d = h / Hg, hl = h % Hg;
+  const int rows_heads = R * H;
+  const int v = blockIdx.y * kProjVecs + tid;  // this thread's vector = A row = TMEM lane
+  const bool valid = v < num_ranks * R;
+  const int k = valid ? v / R : 0, row = valid ? v % R : 0;
+  const int64_t p0 = (int64_t)k * num_splits * rows_heads + (int64_t)row * H + h;
+
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbarrier_init_cluster();
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, kProjTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = __shfl_sync(0xffffffffu, *tslot, 0);
+
+  // merge weights of this vector's splits: w_s = 2^(m_s - M) l_s / sum
+  float M = -INFINITY, den = 0.f;
+  if (valid) {
+    for (int s = 0; s < num_splits; ++s) M = fmaxf(M, part_m[p0 + (int64_t)s * rows_heads]);
+    if (M != -INFINITY) {
+      for (int s = 0; s < num_splits; ++s) {
+        const float m = part_m[p0 + (int64_t)s * rows_heads];
+        const float l = part_l[p0 + (int64_t)s * rows_heads];
+        if (m != -INFINITY && l > 0.f) den += exp2f(m - M) * l;
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.0f / den : 0.f;
+  const uint32_t idesc = idesc_f16(kProjVecs, P, true, false);
+  const uint32_t sbase = smem_u32(base);
+
+  for (int c = 0; c < kDv / kProjChunk; ++c) {
+    const int st = c & 1;
+    uint8_t* A = base + st * stage_bytes;
+    uint8_t* B = A + kProjABytes;
+    // the MMAs of chunk c-2 read this stage
+    if (c >= 2) proj_wait(&bars[st], ((c - 2) >> 1) & 1, status);
+    float acc[kProjChunk];
+#pragma unroll
+    for (int e = 0; e < kProjChunk; ++e) acc[e] = 0.f;
+    if (den > 0.f) {
+      for (int s = 0; s < num_splits; ++s) {
+        const int64_t i = p0 + (int64_t)s * rows_heads;
+        const float m = part_m[i];
+        const float l = part_l[i];
+        if (m == -INFINITY || !(l > 0.f)) continue;
+        const float w = exp2f(m - M) * l * inv;
+        const float4* src = reinterpret_cast<const float4*>(part_o + i * kDv + c * kProjChunk);
+#pragma unroll
+        for (int q = 0; q < kProjChunk / 4; ++q) {
+          const float4 o = src[q];
+          acc[4 * q] = fmaf(w, o.x, acc[4 * q]);
+          acc[4 * q + 1] = fmaf(w, o.y, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(w, o.z, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(w, o.w, acc[4 * q + 3]);
+        }
+      }
+    }
+    // A row tid: 8 groups of 8 dims, group j at 16-byte slot j ^ (tid & 7)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t wd[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[8 * j + 2 * q], acc[8 * j + 2 * q + 1]);
+        wd[q] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      *reinterpret_cast<uint4*>(A + tid * 128 + ((j ^ (tid & 7)) << 4)) =
+          make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    }
+    // B rows: the chunk's 64 weights of each projected value p
+    for (int pr = tid; pr < P; pr += blockDim.x) {
+      const uint4* src =
+          reinterpret_cast<const uint4*>(w_v + ((int64_t)h * P + pr) * kDv + c * kProjChunk);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(B + pr * 128 + ((j ^ (pr & 7)) << 4)) = src[j];
+    }
+    fence_proxy_async_smem();  // the tensor core reads the tiles (async proxy)
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t a_addr = sbase + st * stage_bytes;
+        const uint32_t b_addr = a_addr + kProjABytes;
+#pragma unroll
+        for (int kk = 0; kk < kProjChunk / 16; ++kk)
+          mma_f16_ss(tbase, smem_desc_sw128(a_addr + kk * 32, 16, 1024),
+                     smem_desc_sw128(b_addr + kk * 32, 16, 1024), idesc,
+                     (c > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&bars[st]);
+      }
+      __syncwarp();
+    }
+  }
+  // chunks 6 and 7 were the fourth commits of their barriers (phase 3)
+  proj_wait(&bars[0], 1, status);
+  proj_wait(&bars[1], 1, status);
+  tc_fence_after();
+
+  uint16_t* chunk = send + ((int64_t)k * G + d) * cw;
+  const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);
+  for (int c16 = 0; c16 < P / 16; ++c16) {
+    uint32_t r[16];
+    tmem_ld16(trow + 16 * c16, r);
+    tmem_wait_ld16(r);
+    if (valid) {
+      uint32_t wd[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[2 * q]),
+                                                  __uint_as_float(r[2 * q + 1]));
+        wd[q] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(chunk + ((int64_t)row * Hg + hl) * P + 16 * c16);
+      dst[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      dst[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+    }
+  }
+  if (valid) {
+    const float lse = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
+    const uint32_t bits = __float_as_uint(lse);
+    uint16_t* lp = chunk + (int64_t)R * Hg * P + ((int64_t)row * Hg + hl) * 2;
+    lp[0] = (uint16_t)(bits & 0xFFFFu);
+    lp[1] = (uint16_t)(bits >> 16);
+  }
+  if (blockIdx.x == 0 && blockIdx.y == 0) {  // the zero words that end every chunk
+    const int64_t used = (int64_t)R * Hg * (P + 2);
+    for (int kd = 0; kd < num_ranks * G; ++kd)
+      for (int64_t w = used + tid; w < cw; w += blockDim.x) send[(int64_t)kd * cw + w] = 0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kProjTmemCols);
+  }
+}
+
+}  // namespace
+
+int64_t a2a_chunk_words(int R, int Hg, int P) {
+  const int64_t lse_words = 2 * (int64_t)R * Hg;
+  return (int64_t)R * Hg * P + (lse_words + 7) / 8 * 8;
+}
+
+cudaError_t launch_a2a_pack(const dcp_mla_dims& d, const Derived& x, int num_ranks,
+                            const float* part_o, const float* part_m, const float* part_l,
+                            void* send, cudaStream_t stream) {
+  const int G = d.dcp;
+  const int64_t cw = a2a_chunk_words(x.rows, d.num_heads / G, kDv);
+  dim3 grid((unsigned)(x.rows * d.num_heads), (unsigned)num_ranks);
+  a2a_pack_kernel<<<grid, 128, 0, stream>>>(x.rows, d.num_heads, G, d.num_splits, cw, part_o,
+                                            part_m, part_l, reinterpret_cast<uint16_t*>(send));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_a2a_pack_projected(const dcp_mla_dims& d, const Derived& x, int num_ranks,
+                                      const float* part_o, const float* part_m,
+                                      const float* part_l, const void* w_v, int payload,
+                                      void* send, uint32_t* status, cudaStream_t stream) {
+  const int G = d.dcp;
+  const int64_t cw = a2a_chunk_words(x.rows, d.num_heads / G, payload);
+  const int smem = max(1024 + 2 * (kProjABytes + payload * 128) + 64, kProjMinSmem);
+  static int attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (attr_set[dev] < smem) {
+    e = cudaFuncSetAttribute(a2a_pack_projected_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = smem;
+  }
+  const int64_t vecs = (int64_t)num_ranks * x.rows;
+  dim3 grid((unsigned)d.num_heads, (unsigned)((vecs + kProjVecs - 1) / kProjVecs));
+  a2a_pack_projected_kernel<<<grid, 128, smem, stream>>>(
+      x.rows, d.num_heads, G, num_ranks, d.num_splits, payload, cw, part_o, part_m, part_l,
+      reinterpret_cast<const uint16_t*>(w_v), reinterpret_cast<uint16_t*>(send), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_a2a_combine(const dcp_mla_dims& d, const Derived& x, int payload,
+                               const void* recv, int64_t src_stride, int64_t dst_stride,
+                               int dst_begin, int num_dst, void* out, float* lse,
+                               cudaStream_t stream) {
+  const int G = d.dcp;
+  dim3 grid((unsigned)(x.rows * (d.num_heads / G)), (unsigned)num_dst);
+  a2a_combine_kernel<<<grid, 128, 0, stream>>>(
+      x.rows, d.num_heads, G, payload, reinterpret_cast<const uint16_t*>(recv), src_stride,
+      dst_stride, dst_begin, reinterpret_cast<__nv_bfloat16*>(out), lse);
+  return cudaGetLastError();
+}
+
+}  // namespace dcpmla

@@ -264,6 +264,61 @@ dcp_status dcp_kv_write(const dcp_mla_dims* dims, const int32_t* slot_mapping, c
                         dcp_kv_dtype kv_dtype, const float* kv_scale, int32_t num_ranks,
                         void* pool, uint32_t* status, dcp_stream_t stream);
 
+/*
+ * The step after the path: the cross-rank exchange in the all-to-all wire
+ * format, and project-before-merge.
+ * Defined by: "Context Parallel Guide (PCP & DCP)", "Decode" (each rank returns
+ * its output and LSE; they are LSE-corrected and summed so that every rank ends
+ * with its slice of the heads), "comm_backend" (a2a: one all-to-all with the LSE
+ * packed alongside the output, the fp32 LSE carried as two 16-bit halves of the
+ * BF16 buffer, combine done locally) and "enable_project_before_merge" (a
+ * per-head W_V applied before the merge commutes with it and shrinks the payload
+ * from kv_lora_rank to v_head_dim values per head).
+ *
+ * Wire format. Destination rank d (of G = dims->dcp) owns heads [d*Hg, (d+1)*Hg),
+ * Hg = H / G (H must be a multiple of G). The chunk a source sends to d is
+ * dcp_a2a_chunk_words(dims, P) 16-bit words: [R][Hg][P] BF16 outputs (P =
+ * payload: 512, or the projected width), then [R][Hg][2] LSE words (the low then
+ * the high 16 bits of the float32 natural-log LSE, -inf for an empty rank), then
+ * zero words up to a multiple of 8. A source's send buffer is [G][chunk]: an
+ * all-to-all of equal splits delivers send_s[d] to rank d as its recv[s].
+ *
+ * dcp_a2a_chunk_words: words of one chunk; -1 if dims or payload are invalid.
+ *
+ * dcp_a2a_pack: for each rank k < num_ranks of the partials (dcp_mla_partial's
+ * outputs), merges its splits into its normalised output O_k and its LSE_k and
+ * writes them into its send buffer.
+ *   w_v      NULL: payload must be 512 and O_k is sent rounded to BF16 (nearest
+ *            even). Else device bf16 [H][payload][512] (row p of head h is the
+ *            512 weights of projected value p) and payload is a multiple of 16
+ *            in [16, 256]: O_k is rounded to BF16, projected on the tensor cores
+ *            (fp32 accumulation) and the projection is sent rounded to BF16.
+ *   send     device, 16-byte aligned, [num_ranks][G][chunk words]     out
+ *   status   device uint32 [1] or NULL: DCP_STATUS_TIMEOUT if a wait on the
+ *            tensor cores gives up (bounded; projected form only)
+ *
+ * dcp_a2a_combine: for destination ranks dst_begin .. dst_begin+num_dst-1, the
+ * combine of the G chunks each received:
+ *   LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s (0 and -inf if
+ *   every source is empty).
+ *   recv        device, 16-byte aligned: the chunk from source s to destination
+ *               dst_begin+i starts at word i*dst_stride + s*src_stride (both
+ *               multiples of 8). After a real all-to-all each rank passes its own
+ *               recv buffer (num_dst 1, src_stride = chunk words); with all ranks
+ *               on one device the send buffers of dcp_a2a_pack serve directly
+ *               (src_stride = G*chunk words, dst_stride = chunk words).
+ *   out         device bf16 [R][H][payload]: the destinations' heads are written
+ *   lse         device float [R][H]: the destinations' heads are written
+ */
+int64_t dcp_a2a_chunk_words(const dcp_mla_dims* dims, int32_t payload);
+dcp_status dcp_a2a_pack(const dcp_mla_dims* dims, int32_t num_ranks, const float* part_o,
+                        const float* part_m, const float* part_l, const void* w_v,
+                        int32_t payload, void* send, uint32_t* status, dcp_stream_t stream);
+dcp_status dcp_a2a_combine(const dcp_mla_dims* dims, int32_t payload, const void* recv,
+                           int64_t src_stride, int64_t dst_stride, int32_t dst_begin,
+                           int32_t num_dst, void* out, float* lse, uint32_t* status,
+                           dcp_stream_t stream);
+
 /* Message for the last non-OK return on this thread ("" if none). */
 const char* dcp_last_error(void);
 

@@ -111,3 +111,30 @@ def test_max_pages(dm):
                                       max_blocks_per_seq=2048)) == 2048
     assert dm.dcp_mla_max_pages(_dims(dm, max_local_len=300, block_size=96,
                                       max_blocks_per_seq=4)) == 10
+
+
+def test_a2a_chunk_words_and_argument_checks(dm):
+    lib = dm.load()
+    d = _dims(dm, batch=4, qlen=3, num_heads=128, dcp=8, block_size=64, max_blocks_per_seq=2048,
+              max_local_len=131072)
+    # 12 rows x 16 heads x (512 outputs + 2 LSE words), already a multiple of 8
+    assert dm.dcp_a2a_chunk_words(d) == 12 * 16 * 514
+    assert dm.dcp_a2a_chunk_words(d, 128) == 12 * 16 * 130
+    small = _dims(dm, batch=1, qlen=3, num_heads=2, dcp=2)  # 3 x 1 x 2 LSE words -> padded
+    assert dm.dcp_a2a_chunk_words(small) == 3 * 512 + 8
+    assert lib.dcp_a2a_chunk_words(ctypes.byref(_dims(dm, num_heads=6, dcp=4)), 512) == -1
+    assert lib.dcp_a2a_chunk_words(ctypes.byref(d), 0) == -1
+    # payload must be 512 without a projection, a multiple of 16 in [16, 256] with one
+    rc = lib.dcp_a2a_pack(ctypes.byref(d), 8, None, None, None, None, 128, None, None, None)
+    assert rc == dm.DCP_ERR_INVALID_ARG and "payload" in dm.dcp_last_error()
+    rc = lib.dcp_a2a_pack(ctypes.byref(d), 8, None, None, None, 16, 100, None, None, None)
+    assert rc == dm.DCP_ERR_INVALID_ARG and "multiple of 16" in dm.dcp_last_error()
+    rc = lib.dcp_a2a_pack(ctypes.byref(d), 8, None, None, None, None, 512, None, None, None)
+    assert rc == dm.DCP_ERR_INVALID_ARG and "NULL" in dm.dcp_last_error()
+    rc = lib.dcp_a2a_pack(ctypes.byref(_dims(dm, num_heads=6, dcp=4)), 4, None, None, None,
+                          None, 512, None, None, None)
+    assert rc == dm.DCP_ERR_INVALID_ARG and "multiple of dcp" in dm.dcp_last_error()
+    rc = lib.dcp_a2a_combine(ctypes.byref(d), 512, None, 12, 0, 0, 1, None, None, None, None)
+    assert rc == dm.DCP_ERR_INVALID_ARG and "strides" in dm.dcp_last_error()
+    rc = lib.dcp_a2a_combine(ctypes.byref(d), 512, None, 8, 0, 7, 2, None, None, None, None)
+    assert rc == dm.DCP_ERR_INVALID_ARG  # destinations beyond dcp

@@ -203,3 +203,12 @@ def generate(name: str = "c1", *, device="cpu", seed_index: Optional[int] = None
         seq_lens=torch.as_tensor(lens, dtype=torch.int32).to(device),
         block_table=torch.as_tensor(table, dtype=torch.int32).to(device),
         q=q, kv=kv)
+
+
+def generate_w_v(num_heads: int, payload: int = 128, seed: int = 7, device="cpu") -> torch.Tensor:
+    """Synthetic per-head value projection for project-before-merge: bf16
+    ``[H][payload][512]`` (row p of head h holds the 512 weights of projected
+    value p), N(0, 1/512) so that projected values keep the scale of the latent
+    ones. Drawn on the host, so every device sees the same weights."""
+    x = _normal((num_heads, payload, 512), _seed(9100, seed), "cpu") / math.sqrt(512)
+    return x.to(torch.bfloat16).to(device)
