@@ -349,31 +349,38 @@ def main():
         nr, R, H = w.dcp, w.rows, w.num_heads
         for label, wv in (("plain", None), ("project_before_merge", w_v)):
             ex = dm.A2AExchange(step, w_v=wv)
-            a_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+            a_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
             for i in range(args.warmup + K):
-                if i >= args.warmup:
-                    a_ev[i - args.warmup][0].record(stream)
-                ex.pack(stream)
-                if i >= args.warmup:
-                    a_ev[i - args.warmup][1].record(stream)
+                e = a_ev[i - args.warmup] if i >= args.warmup else None
+                if e:
+                    e[0].record(stream)
+                ex.pack_ranks(stream)
+                if e:
+                    e[1].record(stream)
+                if wv is not None:
+                    ex.project(stream)
+                if e:
+                    e[2].record(stream)
                 ex.combine_local(stream)
-                if i >= args.warmup:
-                    a_ev[i - args.warmup][2].record(stream)
+                if e:
+                    e[3].record(stream)
             torch.cuda.synchronize()
             if step.read_status() != 0:
                 raise RuntimeError(f"a2a status {step.read_status():#x}")
-            pack_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in a_ev) / K
-            comb_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in a_ev) / K
+            avg = [1e3 * sum(e[j].elapsed_time(e[j + 1]) for e in a_ev) / K for j in range(3)]
+            packed_bytes = ex.packed.numel() * 2
             send_bytes = ex.send.numel() * 2
-            pack_bytes = nr * ns * R * H * (4 * 512 + 8) + send_bytes
+            pack_bytes = nr * ns * R * H * (4 * 512 + 8) + packed_bytes
             comb_bytes = send_bytes + R * H * (2 * ex.payload + 4)
             a2a[label] = {"payload": ex.payload, "send_bytes": send_bytes,
-                          "kernel_us": {"pack": pack_us, "combine": comb_us},
-                          "pack_hbm_gbs": pack_bytes / (pack_us / 1e6) / 1e9,
-                          "combine_hbm_gbs": comb_bytes / (comb_us / 1e6) / 1e9}
+                          "kernel_us": {"pack": avg[0], "combine": avg[2]},
+                          "pack_hbm_gbs": pack_bytes / (avg[0] / 1e6) / 1e9,
+                          "combine_hbm_gbs": comb_bytes / (avg[2] / 1e6) / 1e9}
             if wv is not None:
-                a2a[label]["pack_projection_tflops"] = (
-                    2.0 * nr * R * H * 512 * ex.payload / (pack_us / 1e6) / 1e12)
+                a2a[label]["kernel_us"]["project"] = avg[1]
+                a2a[label]["project_tflops"] = 2.0 * nr * R * H * 512 * ex.payload / (avg[1] / 1e6) / 1e12
+                a2a[label]["project_hbm_gbs"] = (
+                    packed_bytes + wv.numel() * 2 + send_bytes) / (avg[1] / 1e6) / 1e9
             del ex
         a2a["note"] = ("all-to-all wire format (BF16 output + float32 LSE as two 16-bit "
                        "halves), combined on this device; timed separately, not part of "

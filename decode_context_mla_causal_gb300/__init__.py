@@ -13,7 +13,8 @@ from .binding import (  # noqa: F401
     DcpError, Dims, load, library_path,
     dcp_mla_subpage_size, dcp_mla_max_pages, dcp_mla_check_dims,
     dcp_mla_metadata, dcp_mla_partial, dcp_lse_merge, dcp_last_error, dcp_mla_verify_noalloc,
-    dcp_kv_slot_mapping, dcp_kv_write, dcp_a2a_chunk_words, dcp_a2a_pack, dcp_a2a_combine,
+    dcp_kv_slot_mapping, dcp_kv_write, dcp_a2a_chunk_words, dcp_a2a_pack, dcp_a2a_project,
+    dcp_a2a_combine,
 )
 from .step import VerifyStep, choose_num_splits, make_dims, num_sms  # noqa: F401
 from .exchange import A2AExchange, a2a_exchange  # noqa: F401

@@ -88,7 +88,8 @@ def load() -> ctypes.CDLL:
         "dcp_kv_slot_mapping": (I, [D, P, P, I, I, P, P, P]),
         "dcp_kv_write": (I, [D, P, P, I, P, I, P, P, P]),
         "dcp_a2a_chunk_words": (ctypes.c_int64, [D, I]),
-        "dcp_a2a_pack": (I, [D, I, P, P, P, P, I, P, P, P]),
+        "dcp_a2a_pack": (I, [D, I, P, P, P, P, P, P]),
+        "dcp_a2a_project": (I, [D, I, P, P, I, P, P, P]),
         "dcp_a2a_combine": (I, [D, I, P, ctypes.c_int64, ctypes.c_int64, I, I, P, P, P, P]),
         "dcp_last_error": (ctypes.c_char_p, []),
     }
@@ -242,20 +243,33 @@ def dcp_a2a_chunk_words(dims, payload=V_DIM) -> int:
     return int(n)
 
 
-def dcp_a2a_pack(dims, num_ranks, part_o, part_m, part_l, send, w_v=None, payload=V_DIM,
-                 status=None, stream=None):
+def dcp_a2a_pack(dims, num_ranks, part_o, part_m, part_l, send, status=None, stream=None):
     """Each rank's merged output and LSE in the all-to-all wire format (``send`` is a
-    bf16 tensor of ``num_ranks * dcp * chunk_words`` elements); with ``w_v`` (bf16
-    ``[H][payload][512]``) the output is projected first (project-before-merge)."""
+    bf16 tensor of ``num_ranks * dcp * chunk_words`` elements, payload 512)."""
     lib = load()
     R, H = dims.rows, dims.num_heads
     parts = num_ranks * dims.num_splits * R * H
-    cw = dcp_a2a_chunk_words(dims, payload)
+    cw = dcp_a2a_chunk_words(dims, V_DIM)
     _check(lib.dcp_a2a_pack(
         ctypes.byref(dims), int(num_ranks), _ptr(part_o, torch.float32, parts * V_DIM, "part_o"),
         _ptr(part_m, torch.float32, parts, "part_m"), _ptr(part_l, torch.float32, parts, "part_l"),
-        _ptr(w_v, torch.bfloat16, H * payload * V_DIM, "w_v", allow_none=True), int(payload),
         _ptr(send, torch.bfloat16, num_ranks * dims.dcp * cw, "send"),
+        _ptr(status, torch.int32, 1, "status", allow_none=True), _stream(stream)))
+
+
+def dcp_a2a_project(dims, num_ranks, send, w_v, payload, send_projected, status=None,
+                    stream=None):
+    """Project-before-merge of packed send buffers by ``w_v`` (bf16 ``[H][payload][512]``)
+    into ``send_projected`` (payload ``payload``)."""
+    lib = load()
+    H = dims.num_heads
+    cw_in = dcp_a2a_chunk_words(dims, V_DIM)
+    cw = dcp_a2a_chunk_words(dims, payload)
+    _check(lib.dcp_a2a_project(
+        ctypes.byref(dims), int(num_ranks),
+        _ptr(send, torch.bfloat16, num_ranks * dims.dcp * cw_in, "send"),
+        _ptr(w_v, torch.bfloat16, H * payload * V_DIM, "w_v"), int(payload),
+        _ptr(send_projected, torch.bfloat16, num_ranks * dims.dcp * cw, "send_projected"),
         _ptr(status, torch.int32, 1, "status", allow_none=True), _stream(stream)))
 
 

@@ -189,30 +189,44 @@ int64_t dcp_a2a_chunk_words(const dcp_mla_dims* dims, int32_t payload) {
 }
 
 dcp_status dcp_a2a_pack(const dcp_mla_dims* dims, int32_t num_ranks, const float* part_o,
-                        const float* part_m, const float* part_l, const void* w_v,
-                        int32_t payload, void* send, uint32_t* status, dcp_stream_t stream) {
+                        const float* part_m, const float* part_l, void* send, uint32_t* status,
+                        dcp_stream_t stream) {
+  (void)status;
   dcp_status s = check(dims, 0, num_ranks);
   if (s != DCP_OK) return s;
   if (dims->num_heads % dims->dcp != 0)
     return fail(DCP_ERR_INVALID_ARG, "num_heads (%d) must be a multiple of dcp (%d)",
                 dims->num_heads, dims->dcp);
-  if (w_v == nullptr && payload != kDv)
-    return fail(DCP_ERR_INVALID_ARG, "payload must be 512 without w_v (got %d)", payload);
-  if (w_v != nullptr && (payload < 16 || payload > 256 || payload % 16 != 0))
-    return fail(DCP_ERR_INVALID_ARG, "projected payload must be a multiple of 16 in [16, 256]");
   if (dims->batch == 0) return DCP_OK;
   if (!part_o || !part_m || !part_l || !send)
     return fail(DCP_ERR_INVALID_ARG, "dcp_a2a_pack: a required pointer is NULL");
-  if (((uintptr_t)part_o & 15) || ((uintptr_t)send & 15) || ((uintptr_t)w_v & 15))
-    return fail(DCP_ERR_INVALID_ARG, "part_o, send and w_v must be 16-byte aligned");
+  if (((uintptr_t)part_o & 15) || ((uintptr_t)send & 15))
+    return fail(DCP_ERR_INVALID_ARG, "part_o and send must be 16-byte aligned");
   Derived x = derive(*dims);
-  if (w_v == nullptr)
-    return launched(launch_a2a_pack(*dims, x, num_ranks, part_o, part_m, part_l, send,
-                                    (cudaStream_t)stream),
-                    "dcp_a2a_pack");
-  return launched(launch_a2a_pack_projected(*dims, x, num_ranks, part_o, part_m, part_l, w_v,
-                                            payload, send, status, (cudaStream_t)stream),
+  return launched(launch_a2a_pack(*dims, x, num_ranks, part_o, part_m, part_l, send,
+                                  (cudaStream_t)stream),
                   "dcp_a2a_pack");
+}
+
+dcp_status dcp_a2a_project(const dcp_mla_dims* dims, int32_t num_ranks, const void* send,
+                           const void* w_v, int32_t payload, void* send_projected,
+                           uint32_t* status, dcp_stream_t stream) {
+  dcp_status s = check(dims, 0, num_ranks);
+  if (s != DCP_OK) return s;
+  if (dims->num_heads % dims->dcp != 0)
+    return fail(DCP_ERR_INVALID_ARG, "num_heads (%d) must be a multiple of dcp (%d)",
+                dims->num_heads, dims->dcp);
+  if (payload < 16 || payload > 256 || payload % 16 != 0)
+    return fail(DCP_ERR_INVALID_ARG, "projected payload must be a multiple of 16 in [16, 256]");
+  if (dims->batch == 0) return DCP_OK;
+  if (!send || !w_v || !send_projected)
+    return fail(DCP_ERR_INVALID_ARG, "dcp_a2a_project: a required pointer is NULL");
+  if (((uintptr_t)send & 15) || ((uintptr_t)w_v & 15) || ((uintptr_t)send_projected & 15))
+    return fail(DCP_ERR_INVALID_ARG, "send, w_v and send_projected must be 16-byte aligned");
+  Derived x = derive(*dims);
+  return launched(launch_a2a_project(*dims, x, num_ranks, send, w_v, payload, send_projected,
+                                     status, (cudaStream_t)stream),
+                  "dcp_a2a_project");
 }
 
 dcp_status dcp_a2a_combine(const dcp_mla_dims* dims, int32_t payload, const void* recv,

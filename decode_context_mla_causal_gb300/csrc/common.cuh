@@ -56,10 +56,9 @@ cudaError_t launch_a2a_pack(const dcp_mla_dims& d, const Derived& x, int num_ran
                             const float* part_o, const float* part_m, const float* part_l,
                             void* send, cudaStream_t stream);
 
-cudaError_t launch_a2a_pack_projected(const dcp_mla_dims& d, const Derived& x, int num_ranks,
-                                      const float* part_o, const float* part_m,
-                                      const float* part_l, const void* w_v, int payload,
-                                      void* send, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_a2a_project(const dcp_mla_dims& d, const Derived& x, int num_ranks,
+                               const void* send_in, const void* w_v, int payload, void* send,
+                               uint32_t* status, cudaStream_t stream);
 
 cudaError_t launch_a2a_combine(const dcp_mla_dims& d, const Derived& x, int payload,
                                const void* recv, int64_t src_stride, int64_t dst_stride,

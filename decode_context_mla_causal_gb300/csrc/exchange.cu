@@ -21,19 +21,20 @@
 //                       dcp*(2P + 4) B, writes 2P + 4 B per (row, head).
 //
 // Project-before-merge ("enable_project_before_merge" on the same page): each
-// rank's output is projected by the head's W_V before it is sent, so P = the
+// rank's BF16 output is projected by the head's W_V before it is sent, so P = the
 // projected width instead of 512.
 //
-//   a2a_pack_projected_kernel  one CTA per (head, 128 vectors), a vector being one
-//                       (rank, row): D[128][P] = A[128][512] . W_V[h]^T on the
-//                       tensor cores (tcgen05, M = 128, N = P, K = 512 in 8 chunks
-//                       of 64, fp32 accumulator in tensor memory). The A operand is
-//                       built in place: each thread merges its vector's splits for
-//                       the chunk's 64 dims, rounds to BF16 and stores the row into
-//                       the 128-byte-swizzled K-major tile; W_V rows go to the B
+//   a2a_project_kernel  one CTA per (head, 128 vectors), a vector being one (rank,
+//                       row) entry of packed send buffers: D[128][P] =
+//                       A[128][512] . W_V[h]^T on the tensor cores (tcgen05, M = 128,
+//                       N = P, K = 512 in 8 chunks of 64, fp32 accumulator in tensor
+//                       memory). Each thread copies its vector's 128 bytes of the
+//                       chunk into the 128-byte-swizzled K-major A tile (the next
+//                       chunk's loads are in flight meanwhile); W_V rows go to the B
 //                       tile. Two stages: the stores of chunk c overlap the MMAs of
 //                       chunk c-1. The epilogue reads D back (tcgen05.ld), rounds to
-//                       BF16 and writes the wire entries and the LSE halves.
+//                       BF16 and writes the projected entries; the LSE words are
+//                       copied.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -171,10 +172,9 @@ __device__ bool proj_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
 }
 
 __global__ void __launch_bounds__(128)
-a2a_pack_projected_kernel(int R, int H, int G, int num_ranks, int num_splits, int P, int64_t cw,
-                          const float* __restrict__ part_o, const float* __restrict__ part_m,
-                          const float* __restrict__ part_l, const uint16_t* __restrict__ w_v,
-                          uint16_t* __restrict__ send, uint32_t* status) {
+a2a_project_kernel(int R, int H, int G, int num_ranks, int P, int64_t cw_in, int64_t cw,
+                   const uint16_t* __restrict__ send_in, const uint16_t* __restrict__ w_v,
+                   uint16_t* __restrict__ send, uint32_t* status) {
   extern __shared__ unsigned char smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -183,14 +183,14 @@ a2a_pack_projected_kernel(int R, int H, int G, int num_ranks, int num_splits, in
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
   const int tid = threadIdx.x;
   const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
-  const int lane = tid & 31;
   const int h = blockIdx.x;
   const int Hg = H / G, d = h / Hg, hl = h % Hg;
-  const int rows_heads = R * H;
   const int v = blockIdx.y * kProjVecs + tid;  // this thread's vector = A row = TMEM lane
   const bool valid = v < num_ranks * R;
   const int k = valid ? v / R : 0, row = valid ? v % R : 0;
-  const int64_t p0 = (int64_t)k * num_splits * rows_heads + (int64_t)row * H + h;
+  const int64_t entry = (int64_t)row * Hg + hl;
+  const uint16_t* in_chunk = send_in + ((int64_t)k * G + d) * cw_in;
+  const uint4* arow = reinterpret_cast<const uint4*>(in_chunk + entry * kDv);
 
   if (tid == 0) {
     mbar_init(&bars[0], 1);
@@ -205,22 +205,11 @@ a2a_pack_projected_kernel(int R, int H, int G, int num_ranks, int num_splits, in
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = __shfl_sync(0xffffffffu, *tslot, 0);
-
-  // merge weights of this vector's splits: w_s = 2^(m_s - M) l_s / sum
-  float M = -INFINITY, den = 0.f;
-  if (valid) {
-    for (int s = 0; s < num_splits; ++s) M = fmaxf(M, part_m[p0 + (int64_t)s * rows_heads]);
-    if (M != -INFINITY) {
-      for (int s = 0; s < num_splits; ++s) {
-        const float m = part_m[p0 + (int64_t)s * rows_heads];
-        const float l = part_l[p0 + (int64_t)s * rows_heads];
-        if (m != -INFINITY && l > 0.f) den += exp2f(m - M) * l;
-      }
-    }
-  }
-  const float inv = den > 0.f ? 1.0f / den : 0.f;
   const uint32_t idesc = idesc_f16(kProjVecs, P, true, false);
   const uint32_t sbase = smem_u32(base);
+  uint4 cur[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) cur[j] = valid ? arow[j] : make_uint4(0, 0, 0, 0);
 
   for (int c = 0; c < kDv / kProjChunk; ++c) {
     const int st = c & 1;
@@ -228,38 +217,13 @@ a2a_pack_projected_kernel(int R, int H, int G, int num_ranks, int num_splits, in
     uint8_t* B = A + kProjABytes;
     // the MMAs of chunk c-2 read this stage
     if (c >= 2) proj_wait(&bars[st], ((c - 2) >> 1) & 1, status);
-    float acc[kProjChunk];
+    // A row tid: the chunk's 8 groups of 8 dims, group j at 16-byte slot j ^ (tid & 7)
 #pragma unroll
-    for (int e = 0; e < kProjChunk; ++e) acc[e] = 0.f;
-    if (den > 0.f) {
-      for (int s = 0; s < num_splits; ++s) {
-        const int64_t i = p0 + (int64_t)s * rows_heads;
-        const float m = part_m[i];
-        const float l = part_l[i];
-        if (m == -INFINITY || !(l > 0.f)) continue;
-        const float w = exp2f(m - M) * l * inv;
-        const float4* src = reinterpret_cast<const float4*>(part_o + i * kDv + c * kProjChunk);
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<uint4*>(A + tid * 128 + ((j ^ (tid & 7)) << 4)) = cur[j];
+    if (c + 1 < kDv / kProjChunk) {
 #pragma unroll
-        for (int q = 0; q < kProjChunk / 4; ++q) {
-          const float4 o = src[q];
-          acc[4 * q] = fmaf(w, o.x, acc[4 * q]);
-          acc[4 * q + 1] = fmaf(w, o.y, acc[4 * q + 1]);
-          acc[4 * q + 2] = fmaf(w, o.z, acc[4 * q + 2]);
-          acc[4 * q + 3] = fmaf(w, o.w, acc[4 * q + 3]);
-        }
-      }
-    }
-    // A row tid: 8 groups of 8 dims, group j at 16-byte slot j ^ (tid & 7)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t wd[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[8 * j + 2 * q], acc[8 * j + 2 * q + 1]);
-        wd[q] = *reinterpret_cast<uint32_t*>(&b2);
-      }
-      *reinterpret_cast<uint4*>(A + tid * 128 + ((j ^ (tid & 7)) << 4)) =
-          make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      for (int j = 0; j < 8; ++j) cur[j] = valid ? arow[(c + 1) * 8 + j] : make_uint4(0, 0, 0, 0);
     }
     // B rows: the chunk's 64 weights of each projected value p
     for (int pr = tid; pr < P; pr += blockDim.x) {
@@ -306,17 +270,16 @@ a2a_pack_projected_kernel(int R, int H, int G, int num_ranks, int num_splits, in
                                                   __uint_as_float(r[2 * q + 1]));
         wd[q] = *reinterpret_cast<uint32_t*>(&b2);
       }
-      uint4* dst = reinterpret_cast<uint4*>(chunk + ((int64_t)row * Hg + hl) * P + 16 * c16);
+      uint4* dst = reinterpret_cast<uint4*>(chunk + entry * P + 16 * c16);
       dst[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
       dst[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
     }
   }
   if (valid) {
-    const float lse = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
-    const uint32_t bits = __float_as_uint(lse);
-    uint16_t* lp = chunk + (int64_t)R * Hg * P + ((int64_t)row * Hg + hl) * 2;
-    lp[0] = (uint16_t)(bits & 0xFFFFu);
-    lp[1] = (uint16_t)(bits >> 16);
+    const uint16_t* lin = in_chunk + (int64_t)R * Hg * kDv + entry * 2;
+    uint16_t* lp = chunk + (int64_t)R * Hg * P + entry * 2;
+    lp[0] = lin[0];
+    lp[1] = lin[1];
   }
   if (blockIdx.x == 0 && blockIdx.y == 0) {  // the zero words that end every chunk
     const int64_t used = (int64_t)R * Hg * (P + 2);
@@ -349,11 +312,11 @@ cudaError_t launch_a2a_pack(const dcp_mla_dims& d, const Derived& x, int num_ran
   return cudaGetLastError();
 }
 
-cudaError_t launch_a2a_pack_projected(const dcp_mla_dims& d, const Derived& x, int num_ranks,
-                                      const float* part_o, const float* part_m,
-                                      const float* part_l, const void* w_v, int payload,
-                                      void* send, uint32_t* status, cudaStream_t stream) {
+cudaError_t launch_a2a_project(const dcp_mla_dims& d, const Derived& x, int num_ranks,
+                               const void* send_in, const void* w_v, int payload, void* send,
+                               uint32_t* status, cudaStream_t stream) {
   const int G = d.dcp;
+  const int64_t cw_in = a2a_chunk_words(x.rows, d.num_heads / G, kDv);
   const int64_t cw = a2a_chunk_words(x.rows, d.num_heads / G, payload);
   const int smem = max(1024 + 2 * (kProjABytes + payload * 128) + 64, kProjMinSmem);
   static int attr_set[64] = {};
@@ -362,16 +325,17 @@ cudaError_t launch_a2a_pack_projected(const dcp_mla_dims& d, const Derived& x, i
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (attr_set[dev] < smem) {
-    e = cudaFuncSetAttribute(a2a_pack_projected_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(a2a_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = smem;
   }
   const int64_t vecs = (int64_t)num_ranks * x.rows;
   dim3 grid((unsigned)d.num_heads, (unsigned)((vecs + kProjVecs - 1) / kProjVecs));
-  a2a_pack_projected_kernel<<<grid, 128, smem, stream>>>(
-      x.rows, d.num_heads, G, num_ranks, d.num_splits, payload, cw, part_o, part_m, part_l,
-      reinterpret_cast<const uint16_t*>(w_v), reinterpret_cast<uint16_t*>(send), status);
+  a2a_project_kernel<<<grid, 128, smem, stream>>>(
+      x.rows, d.num_heads, G, num_ranks, payload, cw_in, cw,
+      reinterpret_cast<const uint16_t*>(send_in), reinterpret_cast<const uint16_t*>(w_v),
+      reinterpret_cast<uint16_t*>(send), status);
   return cudaGetLastError();
 }
 

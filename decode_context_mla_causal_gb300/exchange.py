@@ -41,16 +41,31 @@ class A2AExchange:
         self.chunk_words = B.dcp_a2a_chunk_words(dims, self.payload)
         dev = step.part_o.device
         R, H = dims.rows, dims.num_heads
-        self.send = torch.empty(step.num_ranks * dims.dcp * self.chunk_words,
-                                dtype=torch.bfloat16, device=dev)
+        n = step.num_ranks * dims.dcp
+        # what is exchanged; with a projection, the per-rank BF16 outputs come first
+        self.send = torch.empty(n * self.chunk_words, dtype=torch.bfloat16, device=dev)
+        self.packed = self.send if w_v is None else torch.empty(
+            n * B.dcp_a2a_chunk_words(dims, B.V_DIM), dtype=torch.bfloat16, device=dev)
         self.out = torch.empty((R, H, self.payload), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((R, H), dtype=torch.float32, device=dev)
 
     def pack(self, stream=None):
         """Each rank's merged (optionally projected) output and LSE into its send buffer."""
+        self.pack_ranks(stream)
+        if self.w_v is not None:
+            self.project(stream)
+
+    def pack_ranks(self, stream=None):
+        """Each rank's merged BF16 output and LSE (payload 512)."""
         s = self.step
-        B.dcp_a2a_pack(s.dims, s.num_ranks, s.part_o, s.part_m, s.part_l, self.send,
-                       w_v=self.w_v, payload=self.payload, status=s.status, stream=stream)
+        B.dcp_a2a_pack(s.dims, s.num_ranks, s.part_o, s.part_m, s.part_l, self.packed,
+                       status=s.status, stream=stream)
+
+    def project(self, stream=None):
+        """Project-before-merge of the packed outputs into the send buffer."""
+        s = self.step
+        B.dcp_a2a_project(s.dims, s.num_ranks, self.packed, self.w_v, self.payload, self.send,
+                          status=s.status, stream=stream)
 
     def combine_local(self, stream=None):
         """All dcp ranks live on this device: every destination's combine, reading

@@ -286,16 +286,22 @@ dcp_status dcp_kv_write(const dcp_mla_dims* dims, const int32_t* slot_mapping, c
  * dcp_a2a_chunk_words: words of one chunk; -1 if dims or payload are invalid.
  *
  * dcp_a2a_pack: for each rank k < num_ranks of the partials (dcp_mla_partial's
- * outputs), merges its splits into its normalised output O_k and its LSE_k and
- * writes them into its send buffer.
- *   w_v      NULL: payload must be 512 and O_k is sent rounded to BF16 (nearest
- *            even). Else device bf16 [H][payload][512] (row p of head h is the
- *            512 weights of projected value p) and payload is a multiple of 16
- *            in [16, 256]: O_k is rounded to BF16, projected on the tensor cores
- *            (fp32 accumulation) and the projection is sent rounded to BF16.
- *   send     device, 16-byte aligned, [num_ranks][G][chunk words]     out
- *   status   device uint32 [1] or NULL: DCP_STATUS_TIMEOUT if a wait on the
- *            tensor cores gives up (bounded; projected form only)
+ * outputs), merges its splits into its normalised output O_k (rounded to BF16,
+ * nearest even) and its LSE_k, and writes them into its send buffer (P = 512).
+ *   send     device, 16-byte aligned, [num_ranks][G][chunk words(512)]   out
+ *   status   unused (may be NULL)
+ *
+ * dcp_a2a_project: project-before-merge of packed send buffers: every BF16
+ * output O_k of send is projected by its head's W_V on the tensor cores (fp32
+ * accumulation), and send_projected receives the projection rounded to BF16
+ * (P = payload) with the same LSE words.
+ *   send            device, 16-byte aligned: dcp_a2a_pack's output    in
+ *   w_v             device bf16 [H][payload][512], 16-byte aligned: row p of
+ *                   head h holds the 512 weights of projected value p
+ *   payload         a multiple of 16 in [16, 256]
+ *   send_projected  device, 16-byte aligned, [num_ranks][G][chunk words(payload)]
+ *   status          device uint32 [1] or NULL: DCP_STATUS_TIMEOUT if a wait on
+ *                   the tensor cores gives up (bounded)
  *
  * dcp_a2a_combine: for destination ranks dst_begin .. dst_begin+num_dst-1, the
  * combine of the G chunks each received:
@@ -312,8 +318,11 @@ dcp_status dcp_kv_write(const dcp_mla_dims* dims, const int32_t* slot_mapping, c
  */
 int64_t dcp_a2a_chunk_words(const dcp_mla_dims* dims, int32_t payload);
 dcp_status dcp_a2a_pack(const dcp_mla_dims* dims, int32_t num_ranks, const float* part_o,
-                        const float* part_m, const float* part_l, const void* w_v,
-                        int32_t payload, void* send, uint32_t* status, dcp_stream_t stream);
+                        const float* part_m, const float* part_l, void* send, uint32_t* status,
+                        dcp_stream_t stream);
+dcp_status dcp_a2a_project(const dcp_mla_dims* dims, int32_t num_ranks, const void* send,
+                           const void* w_v, int32_t payload, void* send_projected,
+                           uint32_t* status, dcp_stream_t stream);
 dcp_status dcp_a2a_combine(const dcp_mla_dims* dims, int32_t payload, const void* recv,
                            int64_t src_stride, int64_t dst_stride, int32_t dst_begin,
                            int32_t num_dst, void* out, float* lse, uint32_t* status,

@@ -124,15 +124,15 @@ def test_a2a_chunk_words_and_argument_checks(dm):
     assert dm.dcp_a2a_chunk_words(small) == 3 * 512 + 8
     assert lib.dcp_a2a_chunk_words(ctypes.byref(_dims(dm, num_heads=6, dcp=4)), 512) == -1
     assert lib.dcp_a2a_chunk_words(ctypes.byref(d), 0) == -1
-    # payload must be 512 without a projection, a multiple of 16 in [16, 256] with one
-    rc = lib.dcp_a2a_pack(ctypes.byref(d), 8, None, None, None, None, 128, None, None, None)
-    assert rc == dm.DCP_ERR_INVALID_ARG and "payload" in dm.dcp_last_error()
-    rc = lib.dcp_a2a_pack(ctypes.byref(d), 8, None, None, None, 16, 100, None, None, None)
+    # the projected payload is a multiple of 16 in [16, 256]
+    rc = lib.dcp_a2a_project(ctypes.byref(d), 8, None, None, 100, None, None, None)
     assert rc == dm.DCP_ERR_INVALID_ARG and "multiple of 16" in dm.dcp_last_error()
-    rc = lib.dcp_a2a_pack(ctypes.byref(d), 8, None, None, None, None, 512, None, None, None)
+    rc = lib.dcp_a2a_project(ctypes.byref(d), 8, None, None, 128, None, None, None)
+    assert rc == dm.DCP_ERR_INVALID_ARG and "NULL" in dm.dcp_last_error()
+    rc = lib.dcp_a2a_pack(ctypes.byref(d), 8, None, None, None, None, None, None)
     assert rc == dm.DCP_ERR_INVALID_ARG and "NULL" in dm.dcp_last_error()
     rc = lib.dcp_a2a_pack(ctypes.byref(_dims(dm, num_heads=6, dcp=4)), 4, None, None, None,
-                          None, 512, None, None, None)
+                          None, None, None)
     assert rc == dm.DCP_ERR_INVALID_ARG and "multiple of dcp" in dm.dcp_last_error()
     rc = lib.dcp_a2a_combine(ctypes.byref(d), 512, None, 12, 0, 0, 1, None, None, None, None)
     assert rc == dm.DCP_ERR_INVALID_ARG and "strides" in dm.dcp_last_error()
