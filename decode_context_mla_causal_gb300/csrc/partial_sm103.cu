@@ -42,9 +42,10 @@
 //               and token half w/4 of every 64-token tile; Q into TMEM, factor
 //               exchange (double-buffered slots), lazy online softmax, P (16-bit)
 //               into TMEM, epilogue for O columns [128*(w/4), +128). The partner
-//               warp's half maximum comes through shared memory behind a per-tile
-//               barrier; a thread keeps its own factors of the previous tile in
-//               shared memory.
+//               warp's half maximum comes through shared memory; its arrival is on
+//               the same barrier that the peer's factors complete, so one wait covers
+//               both. A thread keeps its own factors of the previous tile in shared
+//               memory.
 //   warps 8-11  KV producers: 16-byte loads of the paged cache rows (subpage ids
 //               from the metadata, bounds-checked), FP8 E4M3 -> f16 conversion,
 //               stores into 128-byte-swizzled K-major tiles of a 3-stage ring.
@@ -88,7 +89,8 @@ constexpr int kQAtomBytes = kRows * 128;       // one 64-dim atom of Q (128 rows
 constexpr int kXchEBytes = 2 * 4 * kRows * 16;
 constexpr int kXchSlotBytes = kXchEBytes + 2 * kRows * 4;
 constexpr int kXchSlots = 2;
-constexpr int kMOwnBufs = 3;                            // own half maxima, by tile mod 3
+constexpr int kMOwnBufs = 3;  // own half maxima, by tile mod 3 (a warp writing tile t+3
+                              // has seen every warp's S load of tile t+2, after its read of t)
 constexpr int kMOwnBytes = kMOwnBufs * 2 * kRows * 4;   // [tile%3][half][row] f32
 constexpr int kLCombBytes = 2 * kRows * 4;              // [half][row] f32, epilogue
 constexpr int kEPrevBytes = 2 * kTileN / 2 * kRows * 4;  // own fp32 factors [half][32][row]
@@ -116,10 +118,10 @@ enum {
   kBarPFull,                           // count 8: P written
   kBarODone,                           // P.V completed
   kBarQFull,                           // count 8
-  kBarXFull,                           // [2] the peer's factors are in my slot
+  kBarXFull,                           // [2] count 9: the peer's factors are in my slot and
+                                       // the 8 local warps wrote their half maxima
   kBarXFree = kBarXFull + kXchSlots,   // [2] count 8: the peer consumed what I wrote
-  kBarMOwn = kBarXFree + kXchSlots,    // [3] count 8: own half maxima of a tile written
-  kBarLComb = kBarMOwn + kMOwnBufs,    // count 8: epilogue l halves written
+  kBarLComb = kBarXFree + kXchSlots,   // count 8: epilogue l halves written
   kBarDrainS,
   kBarDrainP,
   kNumBars
@@ -702,10 +704,11 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
         e_cur[c] = fast_exp2(y.x);
         e_cur[c + 1] = fast_exp2(y.y);
       }
-      // own half maximum for the partner warp (same rows, other half)
+      // own half maximum for the partner warp (same rows, other half); the arrival is
+      // on the exchange barrier of tile i, which the partner waits for anyway
       sh.mown[((i % kMOwnBufs) * 2 + h) * kRows + r] = m_cur;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.bars[kBarMOwn + i % kMOwnBufs]);
+      if (lane == 0) mbar_arrive(&sh.bars[kBarXFull + (i & 1)]);
       // send factors (f16 * 2^14) and m to the peer's slot i&1, free since tile i-2
       const int slot = i & 1;
       if (i >= 2 && !wait_warp(kBarXFree + slot, ((i >> 1) - 1) & 1, true)) {
@@ -736,8 +739,7 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
       const int slot = t & 1;
       // one thread arms this use of the slot with its size (the bytes may already be in)
       if (tid == 0) mbar_arrive_expect_tx(&sh.bars[kBarXFull + slot], kXchSlotBytes);
-      if (!wait_warp(kBarXFull + slot, (t >> 1) & 1, true) ||
-          !wait_warp(kBarMOwn + t % kMOwnBufs, (t / kMOwnBufs) & 1, false)) {
+      if (!wait_warp(kBarXFull + slot, (t >> 1) & 1, true)) {
         ok = false;
         break;
       }
@@ -856,10 +858,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&sh.bars[kBarODone], 1);
     mbar_init(&sh.bars[kBarQFull], kSoftWarps);
     for (int i = 0; i < kXchSlots; ++i) {
-      mbar_init(&sh.bars[kBarXFull + i], 1);  // armed by one local thread + the slot's bytes
+      // armed by one local thread with the slot's bytes; the 8 local warps arrive too
+      mbar_init(&sh.bars[kBarXFull + i], 1 + kSoftWarps);
       mbar_init(&sh.bars[kBarXFree + i], kSoftWarps);
     }
-    for (int i = 0; i < kMOwnBufs; ++i) mbar_init(&sh.bars[kBarMOwn + i], kSoftWarps);
     mbar_init(&sh.bars[kBarLComb], kSoftWarps);
     mbar_init(&sh.bars[kBarDrainS], 1);
     mbar_init(&sh.bars[kBarDrainP], 1);
