@@ -425,7 +425,7 @@ def main():
                      "note": "new-token KV write (the step before the verify path), timed "
                              "separately; not part of ms_per_step"},
         "a2a": a2a,
-        "gpu_launches": 3 * K,
+        "gpu_launches": 4 * K,  # metadata, item order, partial, merge
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

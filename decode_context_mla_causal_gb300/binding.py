@@ -82,7 +82,9 @@ def load() -> ctypes.CDLL:
         "dcp_mla_max_pages": (I, [D]),
         "dcp_mla_check_dims": (I, [D, I, I]),
         "dcp_mla_metadata": (I, [D, P, P, I, I, P, P, P, P, P, P]),
-        "dcp_mla_partial": (I, [D, P, P, I, P, ctypes.c_float, I, I, P, P, P, P, P, P, P, P, P]),
+        "dcp_mla_partial": (I, [D, P, P, I, P, ctypes.c_float, I, I, P, P, P, P, P, P, P, P, P,
+                                P]),
+        "dcp_mla_workspace_size": (I, [D, I, ctypes.POINTER(ctypes.c_size_t)]),
         "dcp_lse_merge": (I, [D, I, P, P, P, P, P, P, P, P]),
         "dcp_mla_verify_noalloc": (I, [D, P, P, P, P, I, P, ctypes.c_float, P, P, P, P]),
         "dcp_kv_slot_mapping": (I, [D, P, P, I, I, P, P, P]),
@@ -168,9 +170,19 @@ def dcp_mla_metadata(dims, seq_lens, block_table, rank_begin, num_ranks, row_len
         _ptr(status, i32, 1, "status"), _stream(stream)))
 
 
+def dcp_mla_workspace_size(dims, num_ranks) -> int:
+    """Bytes of device workspace ``dcp_mla_partial`` takes (the longest-first item order)."""
+    n = ctypes.c_size_t(0)
+    _check(load().dcp_mla_workspace_size(ctypes.byref(dims), int(num_ranks), ctypes.byref(n)))
+    return int(n.value)
+
+
 def dcp_mla_partial(dims, q, kv, kv_dtype, kv_scale, softmax_scale, rank_begin, num_ranks,
                     row_len, page_ids, split_beg, split_end, part_o, part_m, part_l, status,
-                    stream=None):
+                    stream=None, workspace=None):
+    """Partial attention of ranks ``rank_begin ..``; ``workspace`` (a device tensor of at
+    least ``dcp_mla_workspace_size`` bytes, optional) lets the call run the work items
+    longest first (same results)."""
     lib = load()
     B, R, H, NS = dims.batch, dims.rows, dims.num_heads, dims.num_splits
     MP = lib.dcp_mla_max_pages(ctypes.byref(dims))
@@ -190,6 +202,7 @@ def dcp_mla_partial(dims, q, kv, kv_dtype, kv_scale, softmax_scale, rank_begin, 
         _ptr(part_o, f32, num_ranks * NS * R * H * V_DIM, "part_o"),
         _ptr(part_m, f32, num_ranks * NS * R * H, "part_m"),
         _ptr(part_l, f32, num_ranks * NS * R * H, "part_l"),
+        _ptr(workspace, None, None, "workspace", allow_none=True),
         _ptr(status, i32, 1, "status"), _stream(stream)))
 
 

@@ -116,7 +116,8 @@ dcp_status dcp_mla_partial(const dcp_mla_dims* dims, const void* q, const void* 
                            int32_t rank_begin, int32_t num_ranks, const int32_t* row_len,
                            const int32_t* page_ids, const int32_t* split_beg,
                            const int32_t* split_end, float* part_o, float* part_m,
-                           float* part_l, uint32_t* status, dcp_stream_t stream) {
+                           float* part_l, void* workspace, uint32_t* status,
+                           dcp_stream_t stream) {
   dcp_status s = check(dims, rank_begin, num_ranks);
   if (s != DCP_OK) return s;
   if (kv_dtype != DCP_KV_BF16 && kv_dtype != DCP_KV_FP8_E4M3)
@@ -127,13 +128,22 @@ dcp_status dcp_mla_partial(const dcp_mla_dims* dims, const void* q, const void* 
   if (!q || !kv || !row_len || !page_ids || !split_beg || !split_end || !part_o || !part_m ||
       !part_l || !status)
     return fail(DCP_ERR_INVALID_ARG, "dcp_mla_partial: a required pointer is NULL");
-  if (((uintptr_t)q & 15) || ((uintptr_t)kv & 15) || ((uintptr_t)part_o & 15))
-    return fail(DCP_ERR_INVALID_ARG, "q, kv and part_o must be 16-byte aligned");
+  if (((uintptr_t)q & 15) || ((uintptr_t)kv & 15) || ((uintptr_t)part_o & 15) ||
+      ((uintptr_t)workspace & 15))
+    return fail(DCP_ERR_INVALID_ARG, "q, kv, part_o and workspace must be 16-byte aligned");
   Derived x = derive(*dims);
   return launched(launch_partial(*dims, x, q, kv, kv_dtype, kv_scale, softmax_scale, num_ranks,
                                  row_len, page_ids, split_beg, split_end, part_o, part_m, part_l,
-                                 status, (cudaStream_t)stream),
+                                 workspace, status, (cudaStream_t)stream),
                   "dcp_mla_partial");
+}
+
+dcp_status dcp_mla_workspace_size(const dcp_mla_dims* dims, int32_t num_ranks, size_t* bytes) {
+  dcp_status s = check(dims, 0, num_ranks);
+  if (s != DCP_OK) return s;
+  if (bytes == nullptr) return fail(DCP_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = partial_workspace_bytes(*dims, num_ranks);
+  return DCP_OK;
 }
 
 dcp_status dcp_lse_merge(const dcp_mla_dims* dims, int32_t num_ranks, const float* part_o,

@@ -35,7 +35,11 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
                            float softmax_scale, int num_ranks, const int32_t* row_len,
                            const int32_t* page_ids, const int32_t* split_beg,
                            const int32_t* split_end, float* part_o, float* part_m,
-                           float* part_l, uint32_t* status, cudaStream_t stream);
+                           float* part_l, void* workspace, uint32_t* status,
+                           cudaStream_t stream);
+
+// Device workspace launch_partial uses for the item order (bytes, 16-byte multiple).
+size_t partial_workspace_bytes(const dcp_mla_dims& d, int num_ranks);
 
 cudaError_t launch_merge(const dcp_mla_dims& d, const Derived& x, int num_ranks,
                          const float* part_o, const float* part_m, const float* part_l,

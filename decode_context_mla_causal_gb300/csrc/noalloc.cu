@@ -34,7 +34,7 @@ void* g_scratch_ptr[kMaxDevices] = {};
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t row_len, page_ids, split_beg, split_end, part_m, part_l, part_o, total;
+  size_t row_len, page_ids, split_beg, split_end, part_m, part_l, part_o, order, total;
 };
 
 Layout layout_for(const dcp_mla_dims& d, const Derived& x) {
@@ -55,6 +55,8 @@ Layout layout_for(const dcp_mla_dims& d, const Derived& x) {
   off += round256(nr * NS * R * H * sizeof(float));
   l.part_o = off;
   off += round256(nr * NS * R * H * kDv * sizeof(float));
+  l.order = off;
+  off += round256(partial_workspace_bytes(d, (int)nr));
   l.total = off;
   return l;
 }
@@ -122,7 +124,8 @@ extern "C" dcp_status dcp_mla_verify_noalloc(const dcp_mla_dims* dims, const int
                       split_end, status, st);
   if (e == cudaSuccess)
     e = launch_partial(*dims, x, q, kv, kv_dtype, kv_scale, softmax_scale, dims->dcp, row_len,
-                       page_ids, split_beg, split_end, part_o, part_m, part_l, status, st);
+                       page_ids, split_beg, split_end, part_o, part_m, part_l, base + l.order,
+                       status, st);
   if (e == cudaSuccess)
     e = launch_merge(*dims, x, dims->dcp, part_o, part_m, part_l, out, lse, nullptr, status, st);
   if (e != cudaSuccess)

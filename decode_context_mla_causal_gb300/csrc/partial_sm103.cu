@@ -144,6 +144,7 @@ struct Params {
   float* part_m;
   float* part_l;
   uint32_t* status;
+  const int32_t* item_order;  // cluster -> work item (longest first), or null: natural order
   float softmax_scale;
   int batch, qlen, H, num_splits, subpage, max_pages, n_row_tiles;
   int64_t pool_rows;  // rows of one rank's pool: num_blocks * block_size
@@ -218,9 +219,11 @@ struct Item {
   int t_start, t_end, n_tiles;
 };
 
-__device__ __forceinline__ Item decode_item(const Params& p, int cluster_id) {
+// Work item `item` (natural order: rank, sequence, split, row tile, the row tile
+// fastest) with its tile range.
+__device__ __forceinline__ Item decode_item(const Params& p, int item) {
   Item it;
-  int rest = cluster_id;
+  int rest = item;
   it.t = rest % p.n_row_tiles;
   rest /= p.n_row_tiles;
   it.s = rest % p.num_splits;
@@ -835,6 +838,66 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
   }
 }
 
+// ----------------------------------------------------------------- schedule
+// The hardware hands clusters out in index order as SMs free up, so items whose
+// tile counts differ widely (sequences of very different lengths) finish unevenly.
+// order_kernel sorts the items by tile count, longest first, which brings list
+// scheduling within a few percent of the ideal makespan. One CTA: a histogram
+// over (clamped) tile counts, an exclusive scan, a scatter. Items with equal counts
+// land in any order; no item's result depends on the cluster that computes it.
+constexpr int kOrderThreads = 1024;
+constexpr int kOrderBuckets = 4096;  // tile counts at or above the last bucket share it
+constexpr int kOrderMaxItems = 1 << 16;
+
+__global__ void __launch_bounds__(kOrderThreads) order_kernel(const Params p, int n_items,
+                                                              int32_t* order) {
+  __shared__ int bucket[kOrderBuckets];
+  __shared__ int warp_total[kOrderThreads / 32];
+  const int tid = threadIdx.x;
+  for (int b = tid; b < kOrderBuckets; b += kOrderThreads) bucket[b] = 0;
+  __syncthreads();
+  auto key_of = [&](int i) {
+    return kOrderBuckets - 1 - min(decode_item(p, i).n_tiles, kOrderBuckets - 1);
+  };
+  for (int i = tid; i < n_items; i += kOrderThreads) atomicAdd(&bucket[key_of(i)], 1);
+  __syncthreads();
+  // exclusive scan of the buckets, 4 per thread
+  constexpr int kPer = kOrderBuckets / kOrderThreads;
+  int cnt[kPer], sum = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    cnt[j] = bucket[tid * kPer + j];
+    sum += cnt[j];
+  }
+  const int lane = tid & 31, wid = tid >> 5;
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_total[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int t = warp_total[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += v;
+    }
+    warp_total[lane] = t;  // inclusive over warps
+  }
+  __syncthreads();
+  int excl = incl - sum + (wid > 0 ? warp_total[wid - 1] : 0);
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    bucket[tid * kPer + j] = excl;
+    excl += cnt[j];
+  }
+  __syncthreads();
+  for (int i = tid; i < n_items; i += kOrderThreads) order[atomicAdd(&bucket[key_of(i)], 1)] = i;
+}
+
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     partial_tc_kernel(const Params p) {
@@ -845,7 +908,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // tcgen05 operands derived from it need no per-lane serialisation
   const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
   const int cta = (int)cluster_ctarank();
-  const Item it = decode_item(p, blockIdx.x >> 1);
+  const int cluster_id = blockIdx.x >> 1;
+  const Item it = decode_item(p, p.item_order ? p.item_order[cluster_id] : cluster_id);
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -911,7 +975,8 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
                            float softmax_scale, int num_ranks, const int32_t* row_len,
                            const int32_t* page_ids, const int32_t* split_beg,
                            const int32_t* split_end, float* part_o, float* part_m,
-                           float* part_l, uint32_t* status, cudaStream_t stream) {
+                           float* part_l, void* workspace, uint32_t* status,
+                           cudaStream_t stream) {
   Params p;
   p.q = reinterpret_cast<const uint16_t*>(q);
   p.kv = reinterpret_cast<const uint8_t*>(kv);
@@ -924,6 +989,7 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
   p.part_m = part_m;
   p.part_l = part_l;
   p.status = status;
+  p.item_order = nullptr;
   p.softmax_scale = softmax_scale;
   p.batch = d.batch;
   p.qlen = d.qlen;
@@ -947,8 +1013,21 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
     if (e != cudaSuccess) return e;
     attr_set[fp8][dev] = true;
   }
+  if (workspace != nullptr && items <= kOrderMaxItems) {
+    int32_t* order = reinterpret_cast<int32_t*>(workspace);
+    order_kernel<<<1, kOrderThreads, 0, stream>>>(p, (int)items, order);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    p.item_order = order;
+  }
   kern<<<(unsigned)(items * 2), kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
+}
+
+size_t partial_workspace_bytes(const dcp_mla_dims& d, int num_ranks) {
+  const int64_t items = (int64_t)((d.qlen * d.num_heads + kRows - 1) / kRows) * d.num_splits *
+                        d.batch * num_ranks;
+  return (size_t)((items * 4 + 15) / 16 * 16);
 }
 
 }  // namespace dcpmla

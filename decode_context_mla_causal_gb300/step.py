@@ -76,6 +76,9 @@ class VerifyStep:
         self.lse = torch.empty((R, H), dtype=f32, device=dev)
         self.rank_lse = torch.empty((nr, R, H), dtype=f32, device=dev) if rank_lse else None
         self.status = torch.zeros(1, dtype=i32, device=dev)
+        # the partial call's item order (longest first)
+        self.workspace = torch.empty(B.dcp_mla_workspace_size(dims, self.num_ranks),
+                                     dtype=torch.uint8, device=dev)
 
     def metadata(self, seq_lens, block_table, stream=None):
         B.dcp_mla_metadata(self.dims, seq_lens, block_table, self.rank_begin, self.num_ranks,
@@ -86,7 +89,7 @@ class VerifyStep:
         B.dcp_mla_partial(self.dims, q, kv, self.kv_dtype, kv_scale, softmax_scale,
                           self.rank_begin, self.num_ranks, self.row_len, self.page_ids,
                           self.split_beg, self.split_end, self.part_o, self.part_m,
-                          self.part_l, self.status, stream)
+                          self.part_l, self.status, stream, workspace=self.workspace)
 
     def merge(self, stream=None):
         B.dcp_lse_merge(self.dims, self.num_ranks, self.part_o, self.part_m, self.part_l,

@@ -168,6 +168,12 @@ dcp_status dcp_mla_metadata(const dcp_mla_dims* dims, const int32_t* seq_lens,
  *               s_t = softmax_scale * kv_scale * log2(e) * (q . k_t) (base 2);
  *               -inf for an empty split
  *   part_l      device float [nr][NS][R][H]  out: l = sum_t 2^(s_t - m)
+ *   workspace   device, 16-byte aligned, dcp_mla_workspace_size(dims, num_ranks)
+ *               bytes, or NULL. The call first orders the work items (rank,
+ *               sequence, split, 128-row tile) by tile count, longest first, so
+ *               that items of very different lengths finish together (up to 65536
+ *               items; beyond that, and with NULL, items run in their natural
+ *               order). The results are bit-identical either way.
  *   status      device uint32 [1]            in/out: DCP_STATUS_BAD_PAGE,
  *               DCP_STATUS_BAD_SPLIT, DCP_STATUS_TIMEOUT, DCP_STATUS_Q_RANGE
  * Tokens at or beyond a row's length, and pages with invalid ids, never reach
@@ -178,7 +184,11 @@ dcp_status dcp_mla_partial(const dcp_mla_dims* dims, const void* q, const void* 
                            int32_t rank_begin, int32_t num_ranks, const int32_t* row_len,
                            const int32_t* page_ids, const int32_t* split_beg,
                            const int32_t* split_end, float* part_o, float* part_m,
-                           float* part_l, uint32_t* status, dcp_stream_t stream);
+                           float* part_l, void* workspace, uint32_t* status,
+                           dcp_stream_t stream);
+
+/* Bytes of device workspace dcp_mla_partial takes for these dims and num_ranks. */
+dcp_status dcp_mla_workspace_size(const dcp_mla_dims* dims, int32_t num_ranks, size_t* bytes);
 
 /*
  * Step 4: LSE merge of all splits of all ranks into the BF16 output.

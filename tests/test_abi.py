@@ -89,12 +89,12 @@ def test_null_pointers_rejected_without_launch(dm):
                               None, None)
     assert rc == dm.DCP_ERR_INVALID_ARG
     rc = lib.dcp_mla_partial(ctypes.byref(d), None, None, 1, None, 0.1, 0, 2, None, None,
-                             None, None, None, None, None, None, None)
+                             None, None, None, None, None, None, None, None)
     assert rc == dm.DCP_ERR_INVALID_ARG
     rc = lib.dcp_lse_merge(ctypes.byref(d), 2, None, None, None, None, None, None, None, None)
     assert rc == dm.DCP_ERR_INVALID_ARG
     rc = lib.dcp_mla_partial(ctypes.byref(d), None, None, 7, None, 0.1, 0, 2, None, None,
-                             None, None, None, None, None, None, None)
+                             None, None, None, None, None, None, None, None)
     assert rc == dm.DCP_ERR_INVALID_ARG and "kv_dtype" in dm.dcp_last_error()
 
 
@@ -138,3 +138,13 @@ def test_a2a_chunk_words_and_argument_checks(dm):
     assert rc == dm.DCP_ERR_INVALID_ARG and "strides" in dm.dcp_last_error()
     rc = lib.dcp_a2a_combine(ctypes.byref(d), 512, None, 8, 0, 7, 2, None, None, None, None)
     assert rc == dm.DCP_ERR_INVALID_ARG  # destinations beyond dcp
+
+
+def test_workspace_size(dm):
+    # one int32 per work item (rank, sequence, split, 128-row tile), 16-byte multiple
+    d = _dims(dm, batch=32, qlen=5, num_heads=128, dcp=8, num_splits=1)
+    assert dm.dcp_mla_workspace_size(d, 8) == 8 * 32 * 1 * 5 * 4
+    d = _dims(dm, batch=1, qlen=3, num_heads=8, dcp=2, num_splits=3)
+    assert dm.dcp_mla_workspace_size(d, 1) == 16  # 3 items, padded
+    lib = dm.load()
+    assert lib.dcp_mla_workspace_size(ctypes.byref(d), 1, None) == dm.DCP_ERR_INVALID_ARG

@@ -242,6 +242,48 @@ def test_per_rank_calls_equal_one_call(dm):
     assert torch.equal(step.out, full.out) and torch.equal(step.lse, full.lse)
 
 
+def _item_tiles(step, w, subpage):
+    """Tile counts of the work items in natural order (rank, sequence, split, row tile)."""
+    R = w.rows
+    rt = -(-(w.qlen * w.num_heads) // 128)
+    row_len = step.row_len.cpu().numpy()
+    beg, end = step.split_beg.cpu().numpy(), step.split_end.cpu().numpy()
+    tiles = []
+    for k in range(step.num_ranks):
+        for b in range(w.batch):
+            for s in range(step.dims.num_splits):
+                for t in range(rt):
+                    r0 = t * 128
+                    r1 = min(w.qlen * w.num_heads, r0 + 128) - 1
+                    js = range(r0 // w.num_heads, r1 // w.num_heads + 1)
+                    max_l = max(int(row_len[k, b * w.qlen + j]) for j in js)
+                    t0 = int(beg[k, b, s]) * subpage
+                    t1 = min(int(end[k, b, s]) * subpage, max_l)
+                    tiles.append(-(-(t1 - t0) // 64) if t1 > t0 else 0)
+    return np.array(tiles)
+
+
+def test_item_order_is_longest_first_and_changes_nothing(dm):
+    w = workload("c4")  # sequence lengths from 5 to 131072: very uneven work items
+    step = h.run_gpu(dm, w)
+    assert step.read_status() == 0
+    tiles = _item_tiles(step, w, dm.dcp_mla_subpage_size(w.block_size))
+    order = step.workspace.view(torch.int32)[: tiles.size].cpu().numpy()
+    assert np.array_equal(np.sort(order), np.arange(tiles.size))
+    assert (np.diff(np.minimum(tiles[order], 4095)) <= 0).all()
+    ordered = [x.clone() for x in (step.part_o, step.part_m, step.part_l, step.out, step.lse)]
+    scale = torch.tensor([w.kv_scale], dtype=torch.float32, device="cuda")
+    dm.dcp_mla_partial(step.dims, w.q, w.kv, step.kv_dtype, scale, w.softmax_scale, 0,
+                       step.num_ranks, step.row_len, step.page_ids, step.split_beg,
+                       step.split_end, step.part_o, step.part_m, step.part_l, step.status)
+    step.merge()
+    torch.cuda.synchronize()
+    assert step.read_status() == 0
+    for a, b in zip(ordered, (step.part_o, step.part_m, step.part_l, step.out, step.lse)):
+        assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a.view(torch.int16),
+                           b.view(torch.int32) if b.dtype == torch.float32 else b.view(torch.int16))
+
+
 def test_device_errors_set_status_and_stay_safe(dm):
     w = workloads.generate("c2", device="cuda", seed_index=73, overrides=dict(
         batch=3, num_heads=16, max_local_len=512), seq_lens=[2, 900, 5000])
