@@ -17,6 +17,7 @@ namespace dcpmla {
 namespace {
 
 constexpr int kMergeThreads = 128;  // 4 dims per thread
+constexpr int kBatch = 4;           // partials whose loads are issued together
 constexpr float kLn2 = 0.6931471805599453f;
 
 __global__ void __launch_bounds__(kMergeThreads)
@@ -32,18 +33,29 @@ merge_kernel(int rows_heads, int num_ranks, int num_splits, const float* __restr
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
   if (M != -INFINITY) {
-    for (int i = 0; i < n; ++i) {
-      const float m = part_m[(int64_t)i * rows_heads + rh];
-      const float l = part_l[(int64_t)i * rows_heads + rh];
-      if (m == -INFINITY || !(l > 0.f)) continue;
-      const float w = exp2f(m - M) * l;
-      den += w;
-      const float4 o =
-          *reinterpret_cast<const float4*>(part_o + ((int64_t)i * rows_heads + rh) * kDv + d);
-      acc.x = fmaf(w, o.x, acc.x);
-      acc.y = fmaf(w, o.y, acc.y);
-      acc.z = fmaf(w, o.z, acc.z);
-      acc.w = fmaf(w, o.w, acc.w);
+    // kBatch partials per step: their loads are all in flight before the first FMA
+    for (int i0 = 0; i0 < n; i0 += kBatch) {
+      float w[kBatch];
+      float4 o[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = i0 + u;
+        const int64_t idx = (int64_t)min(i, n - 1) * rows_heads + rh;
+        const float m = part_m[idx];
+        const float l = part_l[idx];
+        const bool use = i < n && m != -INFINITY && l > 0.f;
+        w[u] = use ? exp2f(m - M) * l : 0.f;
+        const float4 ov = *reinterpret_cast<const float4*>(part_o + idx * kDv + d);
+        o[u] = use ? ov : make_float4(0.f, 0.f, 0.f, 0.f);  // an unused partial adds nothing
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        den += w[u];
+        acc.x = fmaf(w[u], o[u].x, acc.x);
+        acc.y = fmaf(w[u], o[u].y, acc.y);
+        acc.z = fmaf(w[u], o[u].z, acc.z);
+        acc.w = fmaf(w[u], o[u].w, acc.w);
+      }
     }
   }
   const float inv = den > 0.f ? 1.0f / den : 0.f;
