@@ -210,6 +210,14 @@ a2a_project_kernel(int R, int H, int G, int num_ranks, int P, int64_t cw_in, int
   uint4 cur[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) cur[j] = valid ? arow[j] : make_uint4(0, 0, 0, 0);
+  // this thread's W_V rows (p = tid, tid + 128), one chunk ahead like the A row
+  const uint4* wrow = reinterpret_cast<const uint4*>(w_v + ((int64_t)h * P + tid) * kDv);
+  uint4 bcur[2][8];
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      bcur[q][j] = tid + 128 * q < P ? wrow[q * 128 * (kDv / 8) + j] : make_uint4(0, 0, 0, 0);
 
   for (int c = 0; c < kDv / kProjChunk; ++c) {
     const int st = c & 1;
@@ -226,12 +234,22 @@ a2a_project_kernel(int R, int H, int G, int num_ranks, int P, int64_t cw_in, int
       for (int j = 0; j < 8; ++j) cur[j] = valid ? arow[(c + 1) * 8 + j] : make_uint4(0, 0, 0, 0);
     }
     // B rows: the chunk's 64 weights of each projected value p
-    for (int pr = tid; pr < P; pr += blockDim.x) {
-      const uint4* src =
-          reinterpret_cast<const uint4*>(w_v + ((int64_t)h * P + pr) * kDv + c * kProjChunk);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<uint4*>(B + pr * 128 + ((j ^ (pr & 7)) << 4)) = src[j];
+    for (int q = 0; q < 2; ++q) {
+      const int pr = tid + 128 * q;
+      if (pr < P) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(B + pr * 128 + ((j ^ (pr & 7)) << 4)) = bcur[q][j];
+      }
+    }
+    if (c + 1 < kDv / kProjChunk) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          bcur[q][j] = tid + 128 * q < P ? wrow[q * 128 * (kDv / 8) + (c + 1) * 8 + j]
+                                         : make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();  // the tensor core reads the tiles (async proxy)
     tc_fence_before();

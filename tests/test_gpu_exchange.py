@@ -165,3 +165,44 @@ def test_a2a_matches_the_fp32_merge_within_the_wire(dm):
     fin = np.isfinite(lb)
     assert np.array_equal(np.isneginf(la), np.isneginf(lb))
     assert np.abs(la[fin] - lb[fin]).max(initial=0) <= 1e-5
+
+
+def test_graph_capture_of_step_and_exchange(dm):
+    """The verify step plus pack, projection and combine captured in one CUDA graph and
+    replayed with new lengths and queries equals fresh eager calls bit for bit."""
+    w = workloads.generate("c2", device="cuda")
+    w_v = workloads.generate_w_v(w.num_heads, 128, device="cuda")
+    ns = 3
+    step = dm.VerifyStep(h.dims_of(dm, w, ns), h.kv_dtype_of(dm, w), "cuda")
+    ex = dm.A2AExchange(step, w_v=w_v)
+    scale = torch.tensor([w.kv_scale], dtype=torch.float32, device="cuda")
+    seq, q = w.seq_lens.clone(), w.q.clone()
+    stream = torch.cuda.Stream()
+
+    def run():
+        step(q, w.kv, scale, w.softmax_scale, seq, w.block_table)
+        ex.pack()
+        ex.combine_local()
+
+    with torch.cuda.stream(stream):
+        run()  # warm up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        run()
+    rng = np.random.default_rng(9)
+    for trial in range(2):
+        seq.copy_(torch.as_tensor(rng.integers(w.qlen, 4097, size=w.batch), dtype=torch.int32))
+        q.copy_(torch.randn_like(q, dtype=torch.float32).to(torch.bfloat16))
+        graph.replay()
+        torch.cuda.synchronize()
+        got = (ex.out.clone(), ex.lse.clone(), ex.send.clone())
+        fresh = dm.VerifyStep(h.dims_of(dm, w, ns), h.kv_dtype_of(dm, w), "cuda")
+        fex = dm.A2AExchange(fresh, w_v=w_v)
+        fresh(q, w.kv, scale, w.softmax_scale, seq, w.block_table)
+        fex.pack()
+        fex.combine_local()
+        torch.cuda.synchronize()
+        assert torch.equal(got[0].view(torch.int16), fex.out.view(torch.int16))
+        assert torch.equal(got[1], fex.lse)
+        assert torch.equal(got[2].view(torch.int16), fex.send.view(torch.int16))
