@@ -842,24 +842,30 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
 // The hardware hands clusters out in index order as SMs free up, so items whose
 // tile counts differ widely (sequences of very different lengths) finish unevenly.
 // order_kernel sorts the items by tile count, longest first, which brings list
-// scheduling within a few percent of the ideal makespan. One CTA: a histogram
-// over (clamped) tile counts, an exclusive scan, a scatter. Items with equal counts
-// land in any order; no item's result depends on the cluster that computes it.
+// scheduling within a few percent of the ideal makespan. The sort is over groups
+// (rank, sequence, split): a group's row tiles read the same cache rows, so they
+// stay adjacent and run side by side, sharing those rows in L2. One CTA: a
+// histogram over (clamped) group tile counts, an exclusive scan, a scatter. Groups
+// with equal counts land in any order; no item's result depends on the cluster
+// that computes it.
 constexpr int kOrderThreads = 1024;
 constexpr int kOrderBuckets = 4096;  // tile counts at or above the last bucket share it
 constexpr int kOrderMaxItems = 1 << 16;
 
-__global__ void __launch_bounds__(kOrderThreads) order_kernel(const Params p, int n_items,
+__global__ void __launch_bounds__(kOrderThreads) order_kernel(const Params p, int n_groups,
                                                               int32_t* order) {
   __shared__ int bucket[kOrderBuckets];
   __shared__ int warp_total[kOrderThreads / 32];
   const int tid = threadIdx.x;
   for (int b = tid; b < kOrderBuckets; b += kOrderThreads) bucket[b] = 0;
   __syncthreads();
-  auto key_of = [&](int i) {
-    return kOrderBuckets - 1 - min(decode_item(p, i).n_tiles, kOrderBuckets - 1);
+  const int rt = p.n_row_tiles;
+  auto key_of = [&](int g) {
+    int tiles = 0;
+    for (int t = 0; t < rt; ++t) tiles = max(tiles, decode_item(p, g * rt + t).n_tiles);
+    return kOrderBuckets - 1 - min(tiles, kOrderBuckets - 1);
   };
-  for (int i = tid; i < n_items; i += kOrderThreads) atomicAdd(&bucket[key_of(i)], 1);
+  for (int g = tid; g < n_groups; g += kOrderThreads) atomicAdd(&bucket[key_of(g)], 1);
   __syncthreads();
   // exclusive scan of the buckets, 4 per thread
   constexpr int kPer = kOrderBuckets / kOrderThreads;
@@ -895,7 +901,10 @@ __global__ void __launch_bounds__(kOrderThreads) order_kernel(const Params p, in
     excl += cnt[j];
   }
   __syncthreads();
-  for (int i = tid; i < n_items; i += kOrderThreads) order[atomicAdd(&bucket[key_of(i)], 1)] = i;
+  for (int g = tid; g < n_groups; g += kOrderThreads) {
+    const int pos = atomicAdd(&bucket[key_of(g)], 1);
+    for (int t = 0; t < rt; ++t) order[pos * rt + t] = g * rt + t;
+  }
 }
 
 template <bool kFp8>
@@ -1015,7 +1024,7 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
   }
   if (workspace != nullptr && items <= kOrderMaxItems) {
     int32_t* order = reinterpret_cast<int32_t*>(workspace);
-    order_kernel<<<1, kOrderThreads, 0, stream>>>(p, (int)items, order);
+    order_kernel<<<1, kOrderThreads, 0, stream>>>(p, (int)(items / p.n_row_tiles), order);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     p.item_order = order;

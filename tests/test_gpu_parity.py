@@ -264,13 +264,20 @@ def _item_tiles(step, w, subpage):
 
 
 def test_item_order_is_longest_first_and_changes_nothing(dm):
+    """The order kernel sorts groups of row tiles longest first; results are unchanged."""
     w = workload("c4")  # sequence lengths from 5 to 131072: very uneven work items
     step = h.run_gpu(dm, w)
     assert step.read_status() == 0
     tiles = _item_tiles(step, w, dm.dcp_mla_subpage_size(w.block_size))
     order = step.workspace.view(torch.int32)[: tiles.size].cpu().numpy()
     assert np.array_equal(np.sort(order), np.arange(tiles.size))
-    assert (np.diff(np.minimum(tiles[order], 4095)) <= 0).all()
+    # groups (rank, sequence, split) longest first, each group's row tiles adjacent
+    rt = -(-(w.qlen * w.num_heads) // 128)
+    groups = order.reshape(-1, rt)
+    assert (groups == groups[:, :1] + np.arange(rt)[None]).all()
+    assert (groups[:, 0] % rt == 0).all()
+    group_max = np.minimum(tiles.reshape(-1, rt).max(axis=1), 4095)
+    assert (np.diff(group_max[groups[:, 0] // rt]) <= 0).all()
     ordered = [x.clone() for x in (step.part_o, step.part_m, step.part_l, step.out, step.lse)]
     scale = torch.tensor([w.kv_scale], dtype=torch.float32, device="cuda")
     dm.dcp_mla_partial(step.dims, w.q, w.kv, step.kv_dtype, scale, w.softmax_scale, 0,
