@@ -64,8 +64,11 @@
 // fp32 throughout.
 //
 // Every wait is bounded (DCP_STATUS_TIMEOUT and an orderly exit: all roles stop,
-// in-flight MMAs are drained, TMEM is freed). Waiting threads sleep in
-// mbarrier.try_wait instead of spinning. Nothing traps.
+// in-flight MMAs are drained, TMEM is freed). A wait checks once with a plain
+// mbarrier.try_wait, then sleeps in try_wait with a suspend-time hint. Nothing traps.
+//
+// Work items reach clusters longest first (order_kernel, below), so that items of
+// very different lengths finish together.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -84,7 +87,6 @@ constexpr int kStages = 3;     // KV ring depth
 constexpr int kMaxAtoms = 5;   // 64-dim swizzle atoms staged per CTA (CTA1: 320 dims)
 constexpr int kAtomBytes = kTileN * 128;
 constexpr int kStageBytes = kMaxAtoms * kAtomBytes;
-constexpr int kQAtomBytes = kRows * 128;       // one 64-dim atom of Q (128 rows)
 // factor exchange slot: E as f16 [half 2][group 4][row 128][8 values], m as f32 [half][row]
 constexpr int kXchEBytes = 2 * 4 * kRows * 16;
 constexpr int kXchSlotBytes = kXchEBytes + 2 * kRows * 4;
