@@ -47,6 +47,7 @@ using namespace sm103;
 
 constexpr float kLn2 = 0.6931471805599453f;
 
+template <int kBatch>  // splits whose loads are in flight together (1 when there is one)
 __global__ void __launch_bounds__(128)
 a2a_pack_kernel(int R, int H, int G, int num_splits, int64_t cw, const float* __restrict__ part_o,
                 const float* __restrict__ part_m, const float* __restrict__ part_l,
@@ -57,24 +58,52 @@ a2a_pack_kernel(int R, int H, int G, int num_splits, int64_t cw, const float* __
   const int row = rh / H, h = rh % H;
   const int Hg = H / G, d = h / Hg, hl = h % Hg;
   const int64_t p0 = (int64_t)k * num_splits * rows_heads + rh;  // split 0 of this rank
-  float M = -INFINITY;
-  for (int s = 0; s < num_splits; ++s) M = fmaxf(M, part_m[p0 + (int64_t)s * rows_heads]);
   const int dim = threadIdx.x * 4;
+  // one pass with a running maximum: each batch's m, l and o loads are in flight
+  // together, the sums rescaled by 2^(M_old - M_new) when M rises
+  float M = -INFINITY;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < num_splits; ++s) {
-      const int64_t i = p0 + (int64_t)s * rows_heads;
-      const float m = part_m[i];
-      const float l = part_l[i];
-      if (m == -INFINITY || !(l > 0.f)) continue;
-      const float w = exp2f(m - M) * l;
+  for (int s0 = 0; s0 < num_splits; s0 += kBatch) {
+    float m[kBatch], l[kBatch];
+    float4 o[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      m[u] = -INFINITY;
+      l[u] = 0.f;
+      o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s0 + u < num_splits) {  // no load at all past the last split
+        const int64_t i = p0 + (int64_t)(s0 + u) * rows_heads;
+        m[u] = part_m[i];
+        l[u] = part_l[i];
+        o[u] = *reinterpret_cast<const float4*>(part_o + i * kDv + dim);
+      }
+    }
+    float Mb = M;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (!(s0 + u < num_splits && m[u] != -INFINITY && l[u] > 0.f)) m[u] = -INFINITY;
+      Mb = fmaxf(Mb, m[u]);
+    }
+    if (Mb == -INFINITY) continue;
+    if (Mb != M) {
+      const float a = M == -INFINITY ? 0.f : exp2f(M - Mb);
+      den *= a;
+      acc.x *= a;
+      acc.y *= a;
+      acc.z *= a;
+      acc.w *= a;
+      M = Mb;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const float w = m[u] == -INFINITY ? 0.f : exp2f(m[u] - M) * l[u];
+      const float4 ov = m[u] == -INFINITY ? make_float4(0.f, 0.f, 0.f, 0.f) : o[u];
       den += w;
-      const float4 o = *reinterpret_cast<const float4*>(part_o + i * kDv + dim);
-      acc.x = fmaf(w, o.x, acc.x);
-      acc.y = fmaf(w, o.y, acc.y);
-      acc.z = fmaf(w, o.z, acc.z);
-      acc.w = fmaf(w, o.w, acc.w);
+      acc.x = fmaf(w, ov.x, acc.x);
+      acc.y = fmaf(w, ov.y, acc.y);
+      acc.z = fmaf(w, ov.z, acc.z);
+      acc.w = fmaf(w, ov.w, acc.w);
     }
   }
   const float inv = den > 0.f ? 1.0f / den : 0.f;
@@ -115,28 +144,48 @@ a2a_combine_kernel(int R, int H, int G, int P, const uint16_t* __restrict__ recv
     const uint16_t* lp = base + (int64_t)s * src_stride + lse_off;
     return __uint_as_float((uint32_t)lp[0] | ((uint32_t)lp[1] << 16));
   };
+  // one pass with a running maximum over the sources' LSEs (natural log)
   float M = -INFINITY;
-  for (int s = 0; s < G; ++s) M = fmaxf(M, lse_of(s));
   float den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int dim = threadIdx.x * 4;
   const bool active = dim < P;
-  if (M != -INFINITY) {
-    for (int s = 0; s < G; ++s) {
-      const float ls = lse_of(s);
-      if (ls == -INFINITY) continue;
-      const float w = expf(ls - M);
+  constexpr int kBatch = 4;  // sources whose loads are in flight together
+  for (int s0 = 0; s0 < G; s0 += kBatch) {
+    float ls[kBatch];
+    uint2 v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int s = min(s0 + u, G - 1);
+      ls[u] = s0 + u < G ? lse_of(s) : -INFINITY;
+      v[u] = active ? *reinterpret_cast<const uint2*>(base + (int64_t)s * src_stride +
+                                                       (int64_t)e * P + dim)
+                    : make_uint2(0u, 0u);
+    }
+    float Mb = M;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) Mb = fmaxf(Mb, ls[u]);
+    if (Mb == -INFINITY) continue;
+    if (Mb != M) {
+      const float a = M == -INFINITY ? 0.f : expf(M - Mb);
+      den *= a;
+      acc.x *= a;
+      acc.y *= a;
+      acc.z *= a;
+      acc.w *= a;
+      M = Mb;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (ls[u] == -INFINITY) continue;
+      const float w = expf(ls[u] - M);
       den += w;
-      if (active) {
-        const uint2 v =
-            *reinterpret_cast<const uint2*>(base + (int64_t)s * src_stride + (int64_t)e * P + dim);
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-        acc.x = fmaf(w, a.x, acc.x);
-        acc.y = fmaf(w, a.y, acc.y);
-        acc.z = fmaf(w, b.x, acc.z);
-        acc.w = fmaf(w, b.y, acc.w);
-      }
+      const float2 a2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[u].x));
+      const float2 b2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[u].y));
+      acc.x = fmaf(w, a2.x, acc.x);
+      acc.y = fmaf(w, a2.y, acc.y);
+      acc.z = fmaf(w, b2.x, acc.z);
+      acc.w = fmaf(w, b2.y, acc.w);
     }
   }
   const float inv = den > 0.f ? 1.0f / den : 0.f;
@@ -325,8 +374,10 @@ cudaError_t launch_a2a_pack(const dcp_mla_dims& d, const Derived& x, int num_ran
   const int G = d.dcp;
   const int64_t cw = a2a_chunk_words(x.rows, d.num_heads / G, kDv);
   dim3 grid((unsigned)(x.rows * d.num_heads), (unsigned)num_ranks);
-  a2a_pack_kernel<<<grid, 128, 0, stream>>>(x.rows, d.num_heads, G, d.num_splits, cw, part_o,
-                                            part_m, part_l, reinterpret_cast<uint16_t*>(send));
+  // a single split needs no batch (fewer registers, more resident CTAs)
+  auto kern = d.num_splits == 1 ? a2a_pack_kernel<1> : a2a_pack_kernel<4>;
+  kern<<<grid, 128, 0, stream>>>(x.rows, d.num_heads, G, d.num_splits, cw, part_o, part_m, part_l,
+                                 reinterpret_cast<uint16_t*>(send));
   return cudaGetLastError();
 }
 

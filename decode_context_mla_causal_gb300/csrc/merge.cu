@@ -5,7 +5,7 @@
 // verification", Implementation item 3: base-2 partial statistics become a BF16
 // output plus a natural-log LSE. Splits and ranks are merged in one pass: with
 // m, l, o per (rank, split), M = max m, w = 2^(m - M) * l,
-// O = sum w*o / sum w, LSE = (M + log2 sum w) * ln 2.
+// O = sum w*o / sum w, LSE = (M + log2 sum w) * ln 2 (M kept as a running maximum).
 //
 // HBM-bound: one CTA per (row, head) reads nr*NS partial rows of 512 floats with
 // 16-byte coalesced loads and writes 1 KB of BF16.
@@ -27,35 +27,53 @@ merge_kernel(int rows_heads, int num_ranks, int num_splits, const float* __restr
              float* __restrict__ rank_lse) {
   const int rh = blockIdx.x;  // row * H + head
   const int n = num_ranks * num_splits;
-  float M = -INFINITY;
-  for (int i = 0; i < n; ++i) M = fmaxf(M, part_m[(int64_t)i * rows_heads + rh]);
   const int d = threadIdx.x * 4;
+  // one pass with a running maximum M: a batch's m, l and o loads are all in flight
+  // together, and the sums are rescaled by 2^(M_old - M_new) when M rises
+  float M = -INFINITY;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
-  if (M != -INFINITY) {
-    // kBatch partials per step: their loads are all in flight before the first FMA
-    for (int i0 = 0; i0 < n; i0 += kBatch) {
-      float w[kBatch];
-      float4 o[kBatch];
+  for (int i0 = 0; i0 < n; i0 += kBatch) {
+    float m[kBatch], l[kBatch];
+    float4 o[kBatch];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int i = i0 + u;
-        const int64_t idx = (int64_t)min(i, n - 1) * rows_heads + rh;
-        const float m = part_m[idx];
-        const float l = part_l[idx];
-        const bool use = i < n && m != -INFINITY && l > 0.f;
-        w[u] = use ? exp2f(m - M) * l : 0.f;
-        const float4 ov = *reinterpret_cast<const float4*>(part_o + idx * kDv + d);
-        o[u] = use ? ov : make_float4(0.f, 0.f, 0.f, 0.f);  // an unused partial adds nothing
+    for (int u = 0; u < kBatch; ++u) {
+      m[u] = -INFINITY;
+      l[u] = 0.f;
+      o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i0 + u < n) {  // no load at all past the last partial
+        const int64_t idx = (int64_t)(i0 + u) * rows_heads + rh;
+        m[u] = part_m[idx];
+        l[u] = part_l[idx];
+        o[u] = *reinterpret_cast<const float4*>(part_o + idx * kDv + d);
       }
+    }
+    float Mb = M;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        den += w[u];
-        acc.x = fmaf(w[u], o[u].x, acc.x);
-        acc.y = fmaf(w[u], o[u].y, acc.y);
-        acc.z = fmaf(w[u], o[u].z, acc.z);
-        acc.w = fmaf(w[u], o[u].w, acc.w);
-      }
+    for (int u = 0; u < kBatch; ++u) {
+      const bool use = i0 + u < n && m[u] != -INFINITY && l[u] > 0.f;
+      if (!use) m[u] = -INFINITY;
+      Mb = fmaxf(Mb, m[u]);
+    }
+    if (Mb == -INFINITY) continue;  // nothing so far
+    if (Mb != M) {
+      const float a = M == -INFINITY ? 0.f : exp2f(M - Mb);
+      den *= a;
+      acc.x *= a;
+      acc.y *= a;
+      acc.z *= a;
+      acc.w *= a;
+      M = Mb;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const float w = m[u] == -INFINITY ? 0.f : exp2f(m[u] - M) * l[u];
+      const float4 ov = m[u] == -INFINITY ? make_float4(0.f, 0.f, 0.f, 0.f) : o[u];
+      den += w;
+      acc.x = fmaf(w, ov.x, acc.x);
+      acc.y = fmaf(w, ov.y, acc.y);
+      acc.z = fmaf(w, ov.z, acc.z);
+      acc.w = fmaf(w, ov.w, acc.w);
     }
   }
   const float inv = den > 0.f ? 1.0f / den : 0.f;
