@@ -1,0 +1,43 @@
+"""Host-side logic of the package that needs no GPU: the static split count."""
+
+import math
+
+import pytest
+
+from decode_context_mla_causal_gb300.step import choose_num_splits
+
+
+def _cost(ns, batch, qlen, heads, ranks, bound, slots=76):
+    # the model stated in choose_num_splits' docstring, for the brute-force check
+    tiles = max(1, math.ceil(bound / 64))
+    base = max(1, batch * ranks * math.ceil(qlen * heads / 128))
+    return math.ceil(base * ns / slots) * (tiles / ns + 11.0) + 0.5 * ns
+
+
+@pytest.mark.parametrize("shape,want", [
+    ((1, 3, 8, 2, 100, 16), 2),         # tiny
+    ((4, 3, 96, 2, 2048, 64), 3),       # small
+    ((32, 1, 128, 8, 4096, 64), 1),     # decode: 256 items already fill 3.4 waves
+    ((32, 5, 128, 8, 16384, 64), 1),    # spec-verify: 1280 items
+    ((4, 3, 128, 8, 131072, 64), 7),    # long-context: 96 items of 2048 tiles
+])
+def test_split_choices_of_the_workloads(shape, want):
+    assert choose_num_splits(*shape, sms=152) == want
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 1, 8, 1, 64, 16), (1, 3, 128, 8, 1 << 20, 64), (64, 5, 128, 8, 512, 64),
+    (3, 2, 40, 3, 999, 96), (128, 1, 128, 8, 131072, 64)])
+def test_split_choice_is_the_cheapest_in_range(shape):
+    ns = choose_num_splits(*shape, sms=152)
+    tiles = max(1, math.ceil(shape[4] / 64))
+    assert 1 <= ns <= min(64, tiles)
+    best = min(_cost(k, *shape[:5]) for k in range(1, min(64, tiles) + 1))
+    assert _cost(ns, *shape[:5]) == pytest.approx(best)
+
+
+def test_one_long_item_is_split_and_many_items_are_not():
+    # one (rank, sequence, row tile) of 2048 tiles: split until the SMs are busy
+    assert choose_num_splits(1, 1, 128, 1, 131072, 64, sms=152) >= 32
+    # thousands of items already fill many waves: no split
+    assert choose_num_splits(1024, 1, 128, 8, 4096, 64, sms=152) == 1
