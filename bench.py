@@ -248,8 +248,10 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
-                           if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
+    # raw nvidia-smi samples: DCP_CLOCKS_DIR if set (kept), else a temporary file
+    clocks_dir = os.environ.get("DCP_CLOCKS_DIR")
+    sampler = ClockSampler(local, os.path.join(clocks_dir, f"clocks_rank{rank}.csv")
+                           if clocks_dir and os.path.isdir(clocks_dir)
                            else f"/tmp/dcp_clocks_{os.getpid()}.csv")
     with sampler:
         for i in range(K):
