@@ -41,3 +41,41 @@ def test_one_long_item_is_split_and_many_items_are_not():
     assert choose_num_splits(1, 1, 128, 1, 131072, 64, sms=152) >= 32
     # thousands of items already fill many waves: no split
     assert choose_num_splits(1024, 1, 128, 8, 4096, 64, sms=152) == 1
+
+
+@pytest.mark.parametrize("name", ["c1", "c2"])
+def test_algorithmic_counts_follow_their_definitions(name):
+    """bench.py's per-step counts: every global token read once (by the rank that
+    owns it, counted rank by rank), 2 * (576 + 512) flops per (row, head, visible
+    token) with the visible tokens counted per row, the cache bytes of those tokens
+    plus q once and the BF16 output once."""
+    import bench
+    import workloads
+    from oracle import metadata as M
+
+    w = workloads.generate(name, device="cpu")
+    tokens, flops, nbytes = bench.algorithmic(w)
+    lens = [int(x) for x in w.seq_lens.numpy()]
+    owned = sum(M.count_local(L, r, w.dcp, w.interleave) for L in lens for r in range(w.dcp))
+    assert tokens == owned == sum(lens)
+    visible = sum(M.row_boundary(L, w.qlen, j, True) for L in lens for j in range(w.qlen))
+    assert flops == w.num_heads * visible * 2 * (576 + 512)
+    elem = 1 if w.kv_dtype == "fp8" else 2
+    rows = w.batch * w.qlen
+    assert nbytes == owned * 576 * elem + rows * w.num_heads * (576 + 512) * 2
+
+
+def test_long_context_counts():
+    # B4 H128 qlen3 L = 2^20, FP8: the figures the roofline of the bench line rests on
+    import types
+
+    import torch
+
+    import bench
+
+    w = types.SimpleNamespace(seq_lens=torch.full((4,), 1 << 20), num_heads=128, qlen=3,
+                              causal=True, kv_dtype="fp8", batch=4)
+    tokens, flops, nbytes = bench.algorithmic(w)
+    assert tokens == 4 << 20
+    assert flops == 4 * 128 * 2176 * (3 * (1 << 20) - 3)
+    assert nbytes == (4 << 20) * 576 + 12 * 128 * 1088 * 2 == 2419261440
