@@ -494,6 +494,9 @@ __device__ __forceinline__ void run_pv(const Params& p, const Shared& sh, const 
         mma_f16_ts(tbase + kColO, tp + 8 * kk, vdesc0 + (uint64_t)((kk * 2048) >> 4), idp,
                    kk > 0 ? 1u : acc0);
       tc_commit(&sh.bars[kBarODone]);
+      // P.V(j) done is also an arrival on tile j+1's exchange barrier, whose waiters
+      // then know the P buffer is free and O stable without a second wait
+      tc_commit(&sh.bars[kBarXFull + ((j + 1) & 1)]);
       tc_commit(&sh.bars[kBarKvEmpty + (j % kStages)]);
     }
     __syncwarp();
@@ -743,7 +746,10 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
       const int t = i - 1;
       const int slot = t & 1;
       // one thread arms this use of the slot with its size (the bytes may already be in)
-      if (tid == 0) mbar_arrive_expect_tx(&sh.bars[kBarXFull + slot], kXchSlotBytes);
+      if (tid == 0) {
+        mbar_arrive_expect_tx(&sh.bars[kBarXFull + slot], kXchSlotBytes);
+        if (t == 0) mbar_arrive(&sh.bars[kBarXFull + slot]);  // no P.V before tile 0
+      }
       if (!wait_warp(kBarXFull + slot, (t >> 1) & 1, true)) {
         ok = false;
         break;
@@ -765,11 +771,8 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
         l_half *= alpha;
         M = ub;
       }
-      // P.V(t-1) has completed: the P buffer is free and O is stable
-      if (t >= 1 && !wait_warp(kBarODone, (t - 1) & 1, false)) {
-        ok = false;
-        break;
-      }
+      // P.V(t-1) has completed (its commit was an arrival on this tile's exchange
+      // barrier): the P buffer is free and O is stable
       tc_fence_after();
       if (t >= 1 && __any_sync(0xffffffffu, need)) rescale_o(tO, need ? alpha : 1.f);
       // p = E_own * E_peer * 2^(m_own + m_peer - M); both factors carry 2^14. 8 tokens per
@@ -933,8 +936,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&sh.bars[kBarODone], 1);
     mbar_init(&sh.bars[kBarQFull], kSoftWarps);
     for (int i = 0; i < kXchSlots; ++i) {
-      // armed by one local thread with the slot's bytes; the 8 local warps arrive too
-      mbar_init(&sh.bars[kBarXFull + i], 1 + kSoftWarps);
+      // armed by one local thread with the slot's bytes; the 8 local warps arrive, and
+      // the completion of the previous tile's P.V (tile 0: the arming thread again)
+      mbar_init(&sh.bars[kBarXFull + i], 2 + kSoftWarps);
       mbar_init(&sh.bars[kBarXFree + i], kSoftWarps);
     }
     mbar_init(&sh.bars[kBarLComb], kSoftWarps);
