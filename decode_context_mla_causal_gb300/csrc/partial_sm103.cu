@@ -42,10 +42,10 @@
 //               and token half w/4 of every 64-token tile; Q into TMEM, factor
 //               exchange (double-buffered slots), lazy online softmax, P (16-bit)
 //               into TMEM, epilogue for O columns [128*(w/4), +128). The partner
-//               warp's half maximum comes through shared memory; its arrival is on
-//               the same barrier that the peer's factors complete, so one wait covers
-//               both. A thread keeps its own factors of the previous tile in shared
-//               memory.
+//               warp's half maximum comes through shared memory. Its arrival, and the
+//               completion of the previous tile's P.V, are on the same barrier that the
+//               peer's factors complete, so one wait covers all three. A thread keeps
+//               its own factors of the previous tile in shared memory.
 //   warps 8-11  KV producers: 16-byte loads of the paged cache rows (subpage ids
 //               from the metadata, bounds-checked), FP8 E4M3 -> f16 conversion,
 //               stores into 128-byte-swizzled K-major tiles of a 3-stage ring.
@@ -120,8 +120,9 @@ enum {
   kBarPFull,                           // count 8: P written
   kBarODone,                           // P.V completed
   kBarQFull,                           // count 8
-  kBarXFull,                           // [2] count 9: the peer's factors are in my slot and
-                                       // the 8 local warps wrote their half maxima
+  kBarXFull,                           // [2] count 10: the peer's factors are in my slot,
+                                       // the 8 local warps wrote their half maxima and the
+                                       // previous tile's P.V completed
   kBarXFree = kBarXFull + kXchSlots,   // [2] count 8: the peer consumed what I wrote
   kBarLComb = kBarXFree + kXchSlots,   // count 8: epilogue l halves written
   kBarDrainS,
