@@ -17,14 +17,17 @@
 //     the pair is slow (about 18 bytes per cycle per SM each way, measured), so a
 //     CTA does not send x itself: for each (row, 32-token half) it sends its own
 //     maximum m_c and the factors E_c = 2^(x_c - m_c) in f16 (scaled by 2^14, so
-//     values down to 2^-28 keep 11 bits). The receiver forms
-//         p = E_own * E_peer * 2^(m_own + m_peer - M),
-//     where M is the running reference of the row, raised only when the tile
-//     bound max_half(m_own + m_peer) exceeds it by more than 8 (then O and l are
-//     rescaled). The bound is an upper bound of the true maximum, so p <= 2^8.
-//     Relative error of p and l from the f16 factor: at most 2^-11. Both CTAs
-//     agree on M (sums of the same two floats), so their l and P agree to that
-//     error; each CTA normalises its own half of O by its own l.
+//     values down to 2^-28 keep 11 bits), and keeps the same f16 words. Both CTAs
+//     then form bit-identical weights
+//         p = E_own * E_peer * 2^(m_own + m_peer - M)
+//     (the f16 product is exact in f32), where M is the running reference of the
+//     row. The tile bound max_half(m_own + m_peer) is an upper bound of the true
+//     maximum, but it can lie far above it when the two partial scores of the row
+//     disagree (a token large on one span only, another on the other). So M is
+//     raised only when the bound passes M + 15, and then set 7 below the bound: p
+//     stays below 2^15 (finite in f16), and the tile's largest weight stays in f16's
+//     normal range while the bound overestimates the true maximum by up to 21
+//     binades. Relative error of p and l from the two f16 factors: at most 2^-10.
 //   * CTA c stages dims [256c, 256c + 256 + 64c) of every token: its q.k slice,
 //     which also holds its value slice.
 //   * A thread issuing straight-line tcgen05.mma gets about one instruction per
@@ -45,7 +48,7 @@
 //               warp's half maximum comes through shared memory. Its arrival, and the
 //               completion of the previous tile's P.V, are on the same barrier that the
 //               peer's factors complete, so one wait covers all three. A thread keeps
-//               its own factors of the previous tile in shared memory.
+//               its own f16 factors of the last two tiles in shared memory.
 //   warps 8-11  KV producers: 16-byte loads of the paged cache rows (subpage ids
 //               from the metadata, bounds-checked), FP8 E4M3 -> f16 conversion,
 //               stores into 128-byte-swizzled K-major tiles of a 3-stage ring.
@@ -95,7 +98,8 @@ constexpr int kMOwnBufs = 3;  // own half maxima, by tile mod 3 (a warp writing 
                               // has seen every warp's S load of tile t+2, after its read of t)
 constexpr int kMOwnBytes = kMOwnBufs * 2 * kRows * 4;   // [tile%3][half][row] f32
 constexpr int kLCombBytes = 2 * kRows * 4;              // [half][row] f32, epilogue
-constexpr int kEPrevBytes = 2 * kTileN / 2 * kRows * 4;  // own fp32 factors [half][32][row]
+constexpr int kEPrevBytes = 2 * 2 * 4 * kRows * 16;  // own f16 factors, as sent:
+                                                     // [tile%2][half][group 4][row][8]
 // FP8 producer staging: each producer thread's 16-byte chunks of one tile (the
 // tile after next), [chunk][thread], written by cp.async
 constexpr int kRawBytes = kMaxAtoms * 2 * 128 * 16;
@@ -106,7 +110,12 @@ constexpr int kMmaWarpP = 13;
 constexpr int kThreads = 14 * 32;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // P may grow to 2^8 before O is rescaled
+// Lazy reference: M is raised only when the tile bound passes M + kRaiseAbove, and
+// then set kRefBelow under the bound. P <= 2^(bound - M) <= 2^15 stays finite in f16,
+// and right after a raise P <= 2^7, so the largest weight of the tile keeps full f16
+// precision while the bound overestimates the true maximum by up to 21 binades.
+constexpr float kRaiseAbove = 15.0f;
+constexpr float kRefBelow = 7.0f;
 constexpr float kFactorLog2 = 14.0f;       // factors carry 2^14: E down to 2^-28 stays normal in f16
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -158,7 +167,7 @@ struct Shared {
   uint8_t* xch;   // kXchSlots slots
   float* mown;    // own half maxima per tile
   float* lcomb;   // epilogue l halves
-  float* eprev;   // own factors of the tile awaiting the peer's
+  uint4* eprev;   // own factors (f16, as sent) of the last two tiles
   uint8_t* raw;   // FP8 producer staging
   uint64_t* bars;
   uint32_t* tmem_slot;
@@ -173,7 +182,7 @@ __device__ __forceinline__ Shared carve(unsigned char* raw) {
   s.xch = base + kStages * kStageBytes;
   s.mown = reinterpret_cast<float*>(s.xch + kXchSlots * kXchSlotBytes);
   s.lcomb = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s.mown) + kMOwnBytes);
-  s.eprev = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s.lcomb) + kLCombBytes);
+  s.eprev = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(s.lcomb) + kLCombBytes);
   s.raw = reinterpret_cast<uint8_t*>(s.eprev) + kEPrevBytes;
   s.bars = reinterpret_cast<uint64_t*>(s.raw + kRawBytes);
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + kNumBars);
@@ -609,6 +618,20 @@ __device__ __noinline__ uint32_t small_page_mask(uint32_t vis, const int32_t* pa
   return vis;
 }
 
+// Both 16-bit halves of a and b multiplied pairwise into f32 (exact: a product of
+// two f16 values has 22 significant bits).
+__device__ __forceinline__ float2 mul_f16x2_f32(uint32_t a, uint32_t b) {
+  float2 r;
+  asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+      "mov.b32 {a0, a1}, %2;\n\t"
+      "mov.b32 {b0, b1}, %3;\n\t"
+      "fma.rn.f32.f16 %0, a0, b0, 0f00000000;\n\t"
+      "fma.rn.f32.f16 %1, a1, b1, 0f00000000;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(a), "r"(b));
+  return r;
+}
+
 template <bool kFp8, int kAtoms>
 __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, const Item& it,
                                             uint32_t tbase, int tid, int warp) {
@@ -662,9 +685,10 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
   float M = -INFINITY;  // running reference (log2 units), same in both CTAs
   float l_half = 0.f;   // sum of this half's weights
   bool ok = true;
-  // own factors of the tile finished in the back half live in smem (registers are
-  // capped at 128 per thread with 15 warps): [half][group of 4][row] float4
-  float4* eprev = reinterpret_cast<float4*>(sh.eprev) + h * 8 * kRows + r;
+  // own factors (f16, the words sent to the peer) of the last two tiles, in shared
+  // memory (registers are capped at 128 per thread with 14 warps):
+  // [tile%2][half][group 4][row] uint4
+  uint4* eprev = sh.eprev + h * 4 * kRows + r;
   int32_t pg_next = (big_pages && n > 0) ? __ldg(pages + (it.t_start >> lg_sub)) : 0;
   for (int i = 0; i <= n; ++i) {
     // ---------------- front: scores of tile i -> own factors -> peer
@@ -738,6 +762,7 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
         }
         st_async_v4(dst + (uint32_t)(((h * 4 + g) * kRows + r) * 16), w4[0], w4[1], w4[2],
                     w4[3], rbar);
+        eprev[(slot * 8 + g) * kRows] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
       st_async_b32(dst + kXchEBytes + (uint32_t)((h * kRows + r) * 4), __float_as_uint(m_cur),
                    rbar);
@@ -765,37 +790,35 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
       const float ub1 = (mo1 == -INFINITY || mp1 == -INFINITY) ? -INFINITY : mo1 + mp1;
       const float ub = fmaxf(ub0, ub1);
       const float ub_h = h ? ub1 : ub0;
-      const bool need = ub != -INFINITY && (M == -INFINITY || ub > M + kRescaleThreshold);
+      const bool need = ub != -INFINITY && (M == -INFINITY || ub > M + kRaiseAbove);
       float alpha = 1.f;
       if (need) {
-        alpha = M == -INFINITY ? 0.f : fast_exp2(M - ub);
+        const float m_new = ub - kRefBelow;
+        alpha = M == -INFINITY ? 0.f : fast_exp2(M - m_new);
         l_half *= alpha;
-        M = ub;
+        M = m_new;
       }
       // P.V(t-1) has completed (its commit was an arrival on this tile's exchange
       // barrier): the P buffer is free and O is stable
       tc_fence_after();
       if (t >= 1 && __any_sync(0xffffffffu, need)) rescale_o(tO, need ? alpha : 1.f);
-      // p = E_own * E_peer * 2^(m_own + m_peer - M); both factors carry 2^14. 8 tokens per
-      // step (two steps per loop body), read from the peer's slot and this thread's
-      // own-factor buffer
+      // p = E_own * E_peer * 2^(m_own + m_peer - M); both factors carry 2^14 and are the
+      // f16 words that were exchanged, so the two CTAs form bit-identical weights. 8
+      // tokens per step (two steps per loop body)
       const float f = ub_h == -INFINITY ? 0.f : fast_exp2(ub_h - M - 2.0f * kFactorLog2);
       const float2 f2 = make_float2(f, f);
       float2 lsum2 = make_float2(0.f, 0.f);
       const uint4* pe_src = reinterpret_cast<const uint4*>(src) + h * 4 * kRows + r;
+      const uint4* own = eprev + slot * 8 * kRows;
 #pragma unroll 2
       for (int g = 0; g < 4; ++g) {
-        const uint4 pe = pe_src[g * kRows];
-        const float4 own0 = eprev[(2 * g) * kRows];
-        const float4 own1 = eprev[(2 * g + 1) * kRows];
-        const float ow[8] = {own0.x, own0.y, own0.z, own0.w, own1.x, own1.y, own1.z, own1.w};
-        const uint32_t pw[4] = {pe.x, pe.y, pe.z, pe.w};
+        const uint4 a = own[g * kRows], b = pe_src[g * kRows];
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          // two weights at a time (packed fp32): p = (E_own * f) * E_peer
-          const float2 ep = __half22float2(*reinterpret_cast<const __half2*>(&pw[e]));
-          const float2 pp = __fmul2_rn(__fmul2_rn(make_float2(ow[2 * e], ow[2 * e + 1]), f2), ep);
+          // two weights at a time: the exact f32 product of the two f16 factors, times f
+          const float2 pp = __fmul2_rn(mul_f16x2_f32(aw[e], bw[e]), f2);
           // l sums the fp32 weights; the P.V contraction uses P rounded to 16 bits
           lsum2 = __fadd2_rn(lsum2, pp);
           if (kFp8) {
@@ -816,12 +839,6 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.bars[kBarPFull]);
-    }
-    if (i < n) {
-#pragma unroll
-      for (int g = 0; g < 8; ++g)
-        eprev[g * kRows] =
-            make_float4(e_cur[4 * g], e_cur[4 * g + 1], e_cur[4 * g + 2], e_cur[4 * g + 3]);
     }
   }
 

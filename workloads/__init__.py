@@ -212,3 +212,40 @@ def generate_w_v(num_heads: int, payload: int = 128, seed: int = 7, device="cpu"
     ones. Drawn on the host, so every device sees the same weights."""
     x = _normal((num_heads, payload, 512), _seed(9100, seed), "cpu") / math.sqrt(512)
     return x.to(torch.bfloat16).to(device)
+
+
+def make_anticorrelated(w: Workload, *, seed: int = 5, frac: float = 1.0 / 16,
+                        kappa: float = 12.0, noise: float = 0.1) -> Workload:
+    """Rewrite an FP8 workload so that the partial scores over dims [0, 256) and
+    [256, 576) of one row disagree strongly (input construction only).
+
+    q is constant on each span: c_h / 16 on both, with c_h in {0.75, 0.85, 0.95, 1.0}
+    by head. Every cache row (every slot of every rank's pool) independently becomes
+    "first-span dominant" (value ~kappa on dims [0, 256), ~0 on the rest) with
+    probability frac, "second-span dominant" (~0 on [0, 256), ~kappa * 0.8 on the rest)
+    with probability frac, or small (~0 everywhere); N(0, noise) is added to every
+    value before the E4M3 cast, and kv_scale is 1. Where a group of tokens holds one
+    row of each kind, the sum of the two spans' maxima lies far above the largest
+    score of the group.
+    """
+    if w.kv_dtype != "fp8":
+        raise ValueError("FP8 workloads only")
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    W, NB, bs, D = w.kv.shape
+    u = torch.rand((W, NB, bs), generator=g)
+    x = torch.randn((W, NB, bs, D), generator=g) * noise
+    first = (u < frac).unsqueeze(-1)
+    second = ((u >= frac) & (u < 2 * frac)).unsqueeze(-1)
+    span0 = torch.zeros(D, dtype=torch.bool)
+    span0[:256] = True
+    x = x + torch.where(first & span0, torch.tensor(kappa), torch.tensor(0.0))
+    x = x + torch.where(second & ~span0, torch.tensor(0.8 * kappa), torch.tensor(0.0))
+    codes = x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    c = torch.tensor([0.75, 0.85, 0.95, 1.0])[torch.arange(w.num_heads) % 4] / 16.0
+    q = c.view(1, -1, 1).expand(w.rows, w.num_heads, D).clone()
+    out = dataclasses.replace(w)
+    out.kv = codes.to(w.kv.device)
+    out.q = q.to(torch.bfloat16).to(w.q.device)
+    out.kv_scale = 1.0
+    return out
