@@ -118,6 +118,87 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class NvmlSampler:
+    """The same clock fields read through NVML (ctypes, read-only queries) every 5 ms
+    from a thread, so a timed region of a few tens of ms still gets many samples.
+    ``ok`` is False when NVML cannot be loaded; the caller then uses nvidia-smi."""
+
+    # clocks-event-reason bits of the NVML API
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index, period_s=0.005):
+        import ctypes
+        import threading
+        self.ctypes, self.threading = ctypes, threading
+        self.period, self.samples, self.ok = period_s, [], False
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+                return
+            self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.lib, self.h, self.ok = lib, h, True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _read(self):
+        c = self.ctypes
+        mhz, mx, mw, rs = c.c_uint(), c.c_uint(), c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, c.byref(mhz)) != 0:  # 1: SM clock
+            return None
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, c.byref(mx))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, c.byref(mw))
+        self.reason_fn(self.h, c.byref(rs))
+        return mhz.value, mx.value, mw.value / 1000.0, rs.value
+
+    def __enter__(self):
+        self.stop = False
+
+        def loop():
+            import time as _t
+            while not self.stop:
+                r = self._read()
+                if r is not None:
+                    self.samples.append(r)
+                _t.sleep(self.period)
+        self.th = self.threading.Thread(target=loop, daemon=True)
+        self.th.start()
+        return self
+
+    def __exit__(self, *exc):
+        self.stop = True
+        self.th.join(timeout=2)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        reasons = set()
+        for *_, rs in self.samples:
+            for bit, name in self.REASONS.items():
+                if rs & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(x[0] for x in self.samples),
+                "sm_max_mhz": max(x[1] for x in self.samples), "reasons": sorted(reasons),
+                "samples": len(self.samples), "source": "nvml every 5 ms",
+                "power_w_max": max(x[2] for x in self.samples)}
+
+
+def clock_sampler(local, rank):
+    """NVML sampler if NVML loads, else nvidia-smi every 50 ms (raw samples to
+    DCP_CLOCKS_DIR when set)."""
+    s = NvmlSampler(local)
+    if s.ok:
+        return s
+    clocks_dir = os.environ.get("DCP_CLOCKS_DIR")
+    return ClockSampler(local, os.path.join(clocks_dir, f"clocks_rank{rank}.csv")
+                        if clocks_dir and os.path.isdir(clocks_dir)
+                        else f"/tmp/dcp_clocks_{os.getpid()}.csv")
+
+
 def kernel_source_hash():
     import glob
     h = hashlib.sha256()
@@ -161,17 +242,18 @@ def oracle_prepare(w, b=0):
 
 
 def oracle_sample(w, prepared, heads_sample, rows_sample=None):
-    """Time the CPU oracle on sequence 0 for a subset of heads and rows."""
+    """Time the CPU oracle on sequence 0 for a subset of heads and rows; returns the
+    timing and the oracle's output and LSE of the sample."""
     import oracle
 
     heads = list(range(heads_sample))
     rows = [(0, j) for j in range(w.qlen)] if rows_sample is None else rows_sample
     t0 = time.perf_counter()
-    oracle.attention.forward(rows=rows, heads=heads, per_rank=False, **prepared)
+    ref = oracle.attention.forward(rows=rows, heads=heads, per_rank=False, **prepared)
     dt = time.perf_counter() - t0
     L = int(prepared["seq_lens"][0])
     equiv_tokens = L * (len(heads) * len(rows)) / (w.num_heads * w.qlen)
-    return dict(value=equiv_tokens / dt, seconds=dt,
+    return dict(value=equiv_tokens / dt, seconds=dt, ref=ref, heads=heads, rows=rows,
                 sample=(f"sequence 0 ({L} tokens), {len(rows)} of {w.qlen} verify rows, "
                         f"{len(heads)} of {w.num_heads} heads; value = KV tokens x "
                         f"(sampled rows*heads / all rows*heads) / seconds"))
@@ -185,6 +267,108 @@ def oracle_cores():
         return None
 
 
+# Heads of the oracle sample (all verify rows of sequence 0): the same sample for
+# the cpu_baseline leg and the reference arm, sized for a few seconds of CPU work.
+SAMPLE_HEADS = {"c1": 8, "c2": 96, "c3": 128, "c4": 32, "c5": 32}
+BASELINE_SECONDS = 8.0  # the cpu_baseline leg repeats the sample to about this long
+
+
+def cpu_baseline(w, out, lse):
+    """The cpu_baseline leg: time the oracle on the sample (repeated to about
+    BASELINE_SECONDS) and compare the GPU's output on the same rows and heads."""
+    import numpy as np
+
+    prepared = oracle_prepare(w)
+    runs = [oracle_sample(w, prepared, SAMPLE_HEADS[w.name])]
+    while sum(r["seconds"] for r in runs) < BASELINE_SECONDS and len(runs) < 16:
+        runs.append(oracle_sample(w, prepared, SAMPLE_HEADS[w.name]))
+    secs = sum(r["seconds"] for r in runs)
+    value = len(runs) / sum(1.0 / r["value"] for r in runs)
+    r0 = runs[0]
+    o = out.float().cpu().numpy().astype(np.float64)
+    l = lse.cpu().numpy().astype(np.float64)
+    got_o = np.stack([o[b * w.qlen + j][r0["heads"]] for b, j in r0["rows"]])
+    got_l = np.stack([l[b * w.qlen + j][r0["heads"]] for b, j in r0["rows"]])
+    exp_o, exp_l = r0["ref"]["out"], r0["ref"]["lse"]
+    d = np.abs(got_o - exp_o)
+    fin = np.isfinite(exp_l)
+    dl = np.abs(got_l[fin] - exp_l[fin]) if fin.any() else np.zeros(1)
+    parity = {"sample": "the cpu_baseline sample", "max_abs_out": float(d.max()),
+              "n_out": int(d.size), "n_out_over_1e-2": int((d > 1e-2).sum()),
+              "max_abs_lse": float(dl.max()),
+              "neg_inf_lse_match": bool(np.array_equal(np.isneginf(got_l), np.isneginf(exp_l)))}
+    return ({"value": value, "unit": UNIT, "cores": oracle_cores(), "kind": "oracle",
+             "sample": r0["sample"], "seconds": secs, "repeats": len(runs)}, parity)
+
+
+def setup(config, dev, splits=0):
+    import torch
+
+    import decode_context_mla_causal_gb300 as dm
+    import workloads
+
+    w = workloads.generate(config, device=dev)
+    ns = splits or dm.choose_num_splits(w.batch, w.qlen, w.num_heads, w.dcp,
+                                        w.max_local_len, w.block_size, dm.num_sms(dev))
+    dims = dm.make_dims(batch=w.batch, qlen=w.qlen, num_heads=w.num_heads, dcp=w.dcp,
+                        interleave=w.interleave, block_size=w.block_size,
+                        max_blocks_per_seq=w.max_blocks_per_seq, max_local_len=w.max_local_len,
+                        num_blocks=w.num_blocks, num_splits=ns)
+    kvt = dm.KV_FP8_E4M3 if w.kv_dtype == "fp8" else dm.KV_BF16
+    step = dm.VerifyStep(dims, kvt, dev)
+    scale = torch.tensor([w.kv_scale], dtype=torch.float32, device=dev)
+    kv_bytes = w.kv.numel() * w.kv.element_size()
+    flush = None
+    if kv_bytes < 4 * 129 * 2**20:
+        flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=dev)
+    return dict(w=w, ns=ns, dims=dims, kvt=kvt, step=step, scale=scale, flush=flush,
+                kv_bytes=kv_bytes)
+
+
+def time_steps(env, K, warmup, stream):
+    """W untimed steps, then K steps timed with CUDA events on the launch stream
+    (metadata, partial with its item order, merge). Returns per-step lists in ms."""
+    import torch
+
+    w, step, scale, flush = env["w"], env["step"], env["scale"], env["flush"]
+
+    def run():
+        step.metadata(w.seq_lens, w.block_table)
+        step.partial(w.q, w.kv, scale, w.softmax_scale)
+        step.merge()
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    if step.read_status() != 0:
+        raise RuntimeError(f"device status {step.read_status():#x}")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        if flush is not None:
+            flush.fill_(float(i))
+        ev[i][0].record(stream)
+        step.metadata(w.seq_lens, w.block_table)
+        ev[i][1].record(stream)
+        step.partial(w.q, w.kv, scale, w.softmax_scale)
+        ev[i][2].record(stream)
+        step.merge()
+        ev[i][3].record(stream)
+    torch.cuda.synchronize()
+    return dict(step=[ev[i][0].elapsed_time(ev[i][3]) for i in range(K)],
+                meta=[ev[i][0].elapsed_time(ev[i][1]) for i in range(K)],
+                part=[ev[i][1].elapsed_time(ev[i][2]) for i in range(K)],
+                merge=[ev[i][2].elapsed_time(ev[i][3]) for i in range(K)])
+
+
+def roofline(flops, nbytes, part_ms, peaks):
+    tensor_peak = float(peaks["bf16_tflops"])
+    hbm_peak = float(peaks["hbm_gbs"])
+    achieved = flops / (part_ms / 1e3) / 1e12
+    return achieved, tensor_peak, hbm_peak, max(nbytes / (hbm_peak * 1e9),
+                                                flops / (tensor_peak * 1e12)) * 1e3
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -194,7 +378,7 @@ def main():
     ap.add_argument("--config", default="c5", choices=["c1", "c2", "c3", "c4", "c5"])
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--oracle-heads", type=int, default=0)
+    ap.add_argument("--no-per-config", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -216,61 +400,25 @@ def main():
     dev = torch.device("cuda", local)
     import decode_context_mla_causal_gb300 as dm
 
-    w = workloads.generate(args.config, device=dev)
+    env = setup(args.config, dev, args.splits)
+    w, dims, step, scale, kvt, ns, flush = (env[k] for k in
+                                            ("w", "dims", "step", "scale", "kvt", "ns", "flush"))
     tokens, flops, nbytes = algorithmic(w)
-    ns = args.splits or dm.choose_num_splits(w.batch, w.qlen, w.num_heads, w.dcp,
-                                            w.max_local_len, w.block_size, dm.num_sms(dev))
-    dims = dm.make_dims(batch=w.batch, qlen=w.qlen, num_heads=w.num_heads, dcp=w.dcp,
-                        interleave=w.interleave, block_size=w.block_size,
-                        max_blocks_per_seq=w.max_blocks_per_seq, max_local_len=w.max_local_len,
-                        num_blocks=w.num_blocks, num_splits=ns)
-    kvt = dm.KV_FP8_E4M3 if w.kv_dtype == "fp8" else dm.KV_BF16
-    step = dm.VerifyStep(dims, kvt, dev)
-    scale = torch.tensor([w.kv_scale], dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    kv_bytes = w.kv.numel() * w.kv.element_size()
-    flush = None
-    if kv_bytes < 4 * 129 * 2**20:
-        flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=dev)
-
-    def run():
+    K = args.steps
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = clock_sampler(local, rank)
+    for _ in range(args.warmup):  # untimed, before the sampler starts
         step.metadata(w.seq_lens, w.block_table)
         step.partial(w.q, w.kv, scale, w.softmax_scale)
         step.merge()
-
-    for _ in range(args.warmup):
-        run()
-    torch.cuda.synchronize()
-    if step.read_status() != 0:
-        raise RuntimeError(f"device status {step.read_status():#x}")
-    K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    # raw nvidia-smi samples: DCP_CLOCKS_DIR if set (kept), else a temporary file
-    clocks_dir = os.environ.get("DCP_CLOCKS_DIR")
-    sampler = ClockSampler(local, os.path.join(clocks_dir, f"clocks_rank{rank}.csv")
-                           if clocks_dir and os.path.isdir(clocks_dir)
-                           else f"/tmp/dcp_clocks_{os.getpid()}.csv")
     with sampler:
-        for i in range(K):
-            if flush is not None:
-                flush.fill_(float(i))
-            ev[i][0].record(stream)
-            step.metadata(w.seq_lens, w.block_table)
-            ev[i][1].record(stream)
-            step.partial(w.q, w.kv, scale, w.softmax_scale)
-            ev[i][2].record(stream)
-            step.merge()
-            ev[i][3].record(stream)
-        torch.cuda.synchronize()
+        tm = time_steps(env, K, 0, stream)
     if world > 1:
         dist.barrier()
-    step_ms = [ev[i][0].elapsed_time(ev[i][3]) for i in range(K)]
-    part_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    meta_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    merge_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
+    step_ms, part_ms, meta_ms, merge_ms = tm["step"], tm["part"], tm["meta"], tm["merge"]
     total_ms = sum(step_ms)
     t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -278,6 +426,7 @@ def main():
     total_ms = float(t.item())
     ms_per_step = total_ms / K
     value = tokens * world * K / (total_ms / 1e3)
+    out_keep, lse_keep = step.out.clone(), step.lse.clone()
 
     # end to end through the C ABI with host buffers: per step H2D of q, seq_lens,
     # block_table from pinned memory, the three calls, D2H of out and lse
@@ -326,16 +475,18 @@ def main():
     slots = torch.empty((w.dcp, w.rows), dtype=torch.int32, device=dev)
     kv_status = torch.zeros(1, dtype=torch.int32, device=dev)
     kw_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    kv_copy = w.kv.clone()
     for i in range(args.warmup + K):
         if i >= args.warmup:
             kw_ev[i - args.warmup][0].record(stream)
         dm.dcp_kv_slot_mapping(dims, w.seq_lens, w.block_table, 0, w.dcp, slots, kv_status)
         if i >= args.warmup:
             kw_ev[i - args.warmup][1].record(stream)
-        dm.dcp_kv_write(dims, slots, new_rows, kvt, scale, w.dcp, w.kv, kv_status)
+        dm.dcp_kv_write(dims, slots, new_rows, kvt, scale, w.dcp, kv_copy, kv_status)
         if i >= args.warmup:
             kw_ev[i - args.warmup][2].record(stream)
     torch.cuda.synchronize()
+    del kv_copy
     if int(kv_status.item()) != 0:
         raise RuntimeError(f"kv write status {int(kv_status.item()):#x}")
     kv_map_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in kw_ev) / K
@@ -390,10 +541,7 @@ def main():
 
     peaks, src = load_peaks()
     part_avg = sum(part_ms) / K
-    achieved_tf = flops / (part_avg / 1e3) / 1e12
-    tensor_peak = float(peaks["bf16_tflops"])
-    hbm_peak = float(peaks["hbm_gbs"])
-    roof_ms = max(nbytes / (hbm_peak * 1e9), flops / (tensor_peak * 1e12)) * 1e3
+    achieved_tf, tensor_peak, hbm_peak, roof_ms = roofline(flops, nbytes, part_avg, peaks)
     clocks = sampler.summary()
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -406,7 +554,7 @@ def main():
                    "interleave": w.interleave, "num_splits": ns,
                    "parallelism": f"dcp{w.dcp} virtual shards per GPU; replicas x{world}",
                    "l2": ("flushed with a 512 MB write before each timed step" if flush is not None
-                          else f"inputs larger than L2 (cache {kv_bytes / 1e9:.2f} GB)")},
+                          else f"inputs larger than L2 (cache {env['kv_bytes'] / 1e9:.2f} GB)")},
         "us_per_step": ms_per_step * 1e3,
         "tflops": flops / (ms_per_step / 1e3) / 1e12,
         "kernel_us": {"metadata": 1e3 * sum(meta_ms) / K, "partial": 1e3 * part_avg,
@@ -431,23 +579,59 @@ def main():
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        heads = args.oracle_heads or default_oracle_heads(args.config)
-        cb = oracle_sample(w, oracle_prepare(w), heads)
-        res["cpu_baseline"] = {"value": cb["value"], "unit": UNIT, "cores": oracle_cores(),
-                               "kind": "oracle", "sample": cb["sample"],
-                               "seconds": cb["seconds"]}
+        res["cpu_baseline"], res["parity"] = cpu_baseline(w, out_keep, lse_keep)
+    del env, w, step, out_keep, lse_keep, hq, ho, dq
+    torch.cuda.empty_cache()
+
+    # every other workload of the path at N=1: the same step, timed the same way
+    # (K steps after W untimed ones), with its roofline fraction, the oracle timed on
+    # its sample and the parity of that sample
+    if world == 1 and not args.no_per_config:
+        per = {}
+        sampler2 = clock_sampler(local, rank)
+        with sampler2:
+            for cfg in ("c1", "c2", "c3", "c4", "c5"):
+                if cfg == args.config:
+                    continue
+                e = setup(cfg, dev)
+                cw = e["w"]
+                ctok, cfl, cby = algorithmic(cw)
+                ct = time_steps(e, K, args.warmup, stream)
+                cms = sum(ct["step"]) / K
+                cpart = sum(ct["part"]) / K
+                ach, tp, hp, croof = roofline(cfl, cby, cpart, peaks)
+                entry = {"workload": f"{cfg} {workloads.DESCRIPTIONS[cfg]}",
+                         "num_splits": e["ns"], "ms_per_step": cms,
+                         "value": ctok * K / (sum(ct["step"]) / 1e3), "unit": UNIT,
+                         "tflops": cfl / (cms / 1e3) / 1e12,
+                         "kernel_us": {"metadata": 1e3 * sum(ct["meta"]) / K,
+                                       "partial": 1e3 * cpart,
+                                       "merge": 1e3 * sum(ct["merge"]) / K},
+                         "roofline": {"bound": "tensor", "achieved": ach, "peak": tp,
+                                      "unit": "TFLOP/s", "frac": ach / tp,
+                                      "step_frac": croof / cms,
+                                      "hbm_frac_of_partial":
+                                          cby / (cpart / 1e3) / (hp * 1e9)},
+                         "l2": ("flushed with a 512 MB write before each timed step"
+                                if e["flush"] is not None else "inputs larger than L2")}
+                if not args.no_cpu_baseline:
+                    entry["cpu_baseline"], entry["parity"] = cpu_baseline(
+                        cw, e["step"].out, e["step"].lse)
+                per[cfg] = entry
+                del e, cw
+                torch.cuda.empty_cache()
+        res["per_config"] = per
+        res["per_config_clocks"] = sampler2.summary()
+        res["gpu_launches_per_config"] = 4 * K * len(per)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def default_oracle_heads(config):
-    return {"c1": 8, "c2": 96, "c3": 128, "c4": 128, "c5": 128}[config]
-
-
 def run_reference(args, rank, world):
-    """The CPU oracle as the reference arm (rank 0 only)."""
+    """The CPU oracle as the reference arm (rank 0 only): one step = the oracle on
+    the same sample the cpu_baseline leg of the other arm times."""
     if rank != 0:
         return
     import torch
@@ -456,14 +640,14 @@ def run_reference(args, rank, world):
 
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     w = workloads.generate(args.config, device=dev)
-    heads = args.oracle_heads or max(1, default_oracle_heads(args.config) // 4)
-    rows = [(0, w.qlen - 1)]
+    heads = SAMPLE_HEADS[args.config]
     prepared = oracle_prepare(w)
-    oracle_sample(w, prepared, heads, rows)  # one untimed run (the oracle keeps no state)
+    for _ in range(args.warmup):  # untimed (the oracle keeps no state)
+        oracle_sample(w, prepared, heads)
     vals, secs = [], 0.0
     cb = None
     for _ in range(args.steps):
-        cb = oracle_sample(w, prepared, heads, rows)
+        cb = oracle_sample(w, prepared, heads)
         vals.append(cb["value"])
         secs += cb["seconds"]
     value = len(vals) / sum(1.0 / v for v in vals)

@@ -79,3 +79,19 @@ def test_long_context_counts():
     assert tokens == 4 << 20
     assert flops == 4 * 128 * 2176 * (3 * (1 << 20) - 3)
     assert nbytes == (4 << 20) * 576 + 12 * 128 * 1088 * 2 == 2419261440
+
+
+def test_nvml_sampler_summary_decodes_reason_bits():
+    """The bench's clock summary: median SM clock, maximum, and the clocks-event reason
+    bits of the NVML API mapped to names (samples injected; no GPU or NVML needed)."""
+    import bench
+
+    s = bench.NvmlSampler.__new__(bench.NvmlSampler)
+    s.samples = [(2070, 2070, 900.0, 0), (2070, 2070, 1000.0, 0x4),
+                 (1900, 2070, 1100.0, 0x4 | 0x40), (2070, 2070, 950.0, 0x1)]
+    out = s.summary()
+    assert out["sm_mhz"] == 2070 and out["sm_max_mhz"] == 2070 and out["samples"] == 4
+    assert out["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert out["power_w_max"] == 1100.0
+    s.samples = []
+    assert s.summary()["reasons"] == ["no samples"]
