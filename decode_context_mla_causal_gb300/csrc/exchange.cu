@@ -228,8 +228,10 @@ a2a_project_kernel(int R, int H, int G, int num_ranks, int P, int64_t cw_in, int
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int stage_bytes = kProjABytes + P * 128;  // multiple of 1024 (P % 16 == 0)
+  // bars[0..1]: the MMAs of a stage completed; bars[2]: drain after a timeout
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + 2 * stage_bytes);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   const int tid = threadIdx.x;
   const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
   const int h = blockIdx.x;
@@ -244,6 +246,8 @@ a2a_project_kernel(int R, int H, int G, int num_ranks, int P, int64_t cw_in, int
   if (tid == 0) {
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
+    mbar_init(&bars[2], 1);
+    *abort_flag = 0;
     fence_mbarrier_init_cluster();
   }
   if (warp == 0) {
@@ -272,8 +276,13 @@ a2a_project_kernel(int R, int H, int G, int num_ranks, int P, int64_t cw_in, int
     const int st = c & 1;
     uint8_t* A = base + st * stage_bytes;
     uint8_t* B = A + kProjABytes;
-    // the MMAs of chunk c-2 read this stage
-    if (c >= 2) proj_wait(&bars[st], ((c - 2) >> 1) & 1, status);
+    // the MMAs of chunk c-2 read this stage: one thread waits (bounded), and nobody
+    // writes the stage unless that wait succeeded
+    if (c >= 2) {
+      if (tid == 0 && !proj_wait(&bars[st], ((c - 2) >> 1) & 1, status)) *abort_flag = 1;
+      __syncthreads();
+      if (*abort_flag) break;
+    }
     // A row tid: the chunk's 8 groups of 8 dims, group j at 16-byte slot j ^ (tid & 7)
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -318,14 +327,23 @@ a2a_project_kernel(int R, int H, int G, int num_ranks, int P, int64_t cw_in, int
       __syncwarp();
     }
   }
-  // chunks 6 and 7 were the fourth commits of their barriers (phase 3)
-  proj_wait(&bars[0], 1, status);
-  proj_wait(&bars[1], 1, status);
+  // chunks 6 and 7 were the fourth commits of their barriers (phase 3); after a
+  // timeout, every MMA issued so far is drained instead before TMEM is read or freed
+  if (tid == 0 && !*abort_flag &&
+      !(proj_wait(&bars[0], 1, status) && proj_wait(&bars[1], 1, status)))
+    *abort_flag = 1;
+  __syncthreads();
+  const bool aborted = *abort_flag != 0;
+  if (aborted) {
+    if (warp == 0) tc_commit_elect(&bars[2]);
+    if (tid == 0) proj_wait(&bars[2], 0, status);
+    __syncthreads();
+  }
   tc_fence_after();
 
   uint16_t* chunk = send + ((int64_t)k * G + d) * cw;
   const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);
-  for (int c16 = 0; c16 < P / 16; ++c16) {
+  for (int c16 = 0; c16 < (aborted ? 0 : P / 16); ++c16) {
     uint32_t r[16];
     tmem_ld16(trow + 16 * c16, r);
     tmem_wait_ld16(r);
@@ -342,7 +360,7 @@ a2a_project_kernel(int R, int H, int G, int num_ranks, int P, int64_t cw_in, int
       dst[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
     }
   }
-  if (valid) {
+  if (valid && !aborted) {
     const uint16_t* lin = in_chunk + (int64_t)R * Hg * kDv + entry * 2;
     uint16_t* lp = chunk + (int64_t)R * Hg * P + entry * 2;
     lp[0] = lin[0];

@@ -204,6 +204,8 @@ dcp_status dcp_mla_workspace_size(const dcp_mla_dims* dims, int32_t num_ranks, s
  *             -inf if no rank has a token
  *   rank_lse  device float [nr][R][H]   out (optional, NULL to skip): each
  *             rank's own natural-log LSE, -inf for an empty rank-local row
+ *   status    never written (the merge has no data-dependent failure and no
+ *             wait); kept so the step's calls share one signature; may be NULL
  * With num_ranks < dcp the result merges only the given ranks.
  */
 dcp_status dcp_lse_merge(const dcp_mla_dims* dims, int32_t num_ranks, const float* part_o,
@@ -299,7 +301,7 @@ dcp_status dcp_kv_write(const dcp_mla_dims* dims, const int32_t* slot_mapping, c
  * outputs), merges its splits into its normalised output O_k (rounded to BF16,
  * nearest even) and its LSE_k, and writes them into its send buffer (P = 512).
  *   send     device, 16-byte aligned, [num_ranks][G][chunk words(512)]   out
- *   status   unused (may be NULL)
+ *   status   never written (no data-dependent failure, no wait); may be NULL
  *
  * dcp_a2a_project: project-before-merge of packed send buffers: every BF16
  * output O_k of send is projected by its head's W_V on the tensor cores (fp32
@@ -325,6 +327,7 @@ dcp_status dcp_kv_write(const dcp_mla_dims* dims, const int32_t* slot_mapping, c
  *               (src_stride = G*chunk words, dst_stride = chunk words).
  *   out         device bf16 [R][H][payload]: the destinations' heads are written
  *   lse         device float [R][H]: the destinations' heads are written
+ *   status      never written (no data-dependent failure, no wait); may be NULL
  */
 int64_t dcp_a2a_chunk_words(const dcp_mla_dims* dims, int32_t payload);
 dcp_status dcp_a2a_pack(const dcp_mla_dims* dims, int32_t num_ranks, const float* part_o,

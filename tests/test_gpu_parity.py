@@ -97,10 +97,18 @@ def test_parity_full(dm, name):
     _full_parity(dm, w)
 
 
+# Sampled (sequence, verify row) pairs, every head of each. At H = 128 each verify row
+# is one 128-row tile of the partial kernel, so every row tile is covered, and every
+# row sees every split of its (rank, sequence) pairs. Spec-verify covers a long
+# sequence in full and the short ones (5, 70, 300, 511 tokens) that leave ranks empty.
+ALL_HEADS = list(range(128))
+
+
 @pytest.mark.parametrize("name,rows,heads", [
-    ("c3", [(0, 0), (17, 0), (31, 0)], [0, 1, 63, 127]),
-    ("c4", [(0, 0), (0, 4), (13, 2), (28, 0), (28, 4), (29, 1), (30, 3), (31, 4)], [0, 5, 127]),
-    ("c5", [(0, 0), (0, 2), (3, 1)], [0, 77, 127]),
+    ("c3", [(0, 0), (17, 0), (31, 0)], ALL_HEADS),
+    ("c4", [(0, 0), (0, 1), (0, 2), (0, 3), (0, 4), (13, 2), (28, 0), (28, 4), (29, 1),
+            (30, 3), (31, 4)], ALL_HEADS),
+    ("c5", [(0, 0), (0, 1), (0, 2), (3, 1)], ALL_HEADS),
 ])
 def test_parity_sampled_full_size(dm, name, rows, heads):
     w = workload(name)

@@ -39,13 +39,25 @@ def test_noalloc_matches_allocating_path_twice(dm, name, num_splits):
     ref(w.q, w.kv, scale, w.softmax_scale, w.seq_lens, w.block_table)
     torch.cuda.synchronize()
     assert ref.read_status() == 0
-    for call in range(2):
-        out = torch.full_like(ref.out, float("nan"))
-        lse = torch.full_like(ref.lse, float("nan"))
-        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bufs = [(torch.full_like(ref.out, float("nan")), torch.full_like(ref.lse, float("nan")),
+             torch.zeros(1, dtype=torch.int32, device="cuda")) for _ in range(2)]
+    torch.cuda.synchronize()
+
+    def device_memory():
+        # the driver's free bytes (cudaMemGetInfo) and torch's allocator counters
+        st = torch.cuda.memory_stats()
+        return (torch.cuda.mem_get_info()[0], st.get("allocated_bytes.all.current", 0),
+                st.get("reserved_bytes.all.current", 0))
+
+    for call, (out, lse, status) in enumerate(bufs):
+        before = device_memory()
         dm.dcp_mla_verify_noalloc(dims, w.seq_lens, w.block_table, w.q, w.kv, kvt, scale,
                                   w.softmax_scale, out, lse, status)
         torch.cuda.synchronize()
+        if call == 1:
+            # the first call has looked up the static array's address; a later call
+            # takes no device memory at all
+            assert device_memory() == before
         assert int(status.item()) == 0, call
         st = h.compare(out.float().cpu().numpy(), lse.cpu().numpy(),
                        ref.out.float().cpu().numpy().astype(np.float64),
