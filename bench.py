@@ -301,13 +301,14 @@ def cpu_baseline(w, out, lse):
              "sample": r0["sample"], "seconds": secs, "repeats": len(runs)}, parity)
 
 
-def setup(config, dev, splits=0):
+def setup(config, dev, splits=0, batch=0):
     import torch
 
     import decode_context_mla_causal_gb300 as dm
     import workloads
 
-    w = workloads.generate(config, device=dev)
+    # batch: fewer sequences of the same shape (a small case for profiler captures)
+    w = workloads.generate(config, device=dev, overrides=dict(batch=batch) if batch else None)
     ns = splits or dm.choose_num_splits(w.batch, w.qlen, w.num_heads, w.dcp,
                                         w.max_local_len, w.block_size, dm.num_sms(dev))
     dims = dm.make_dims(batch=w.batch, qlen=w.qlen, num_heads=w.num_heads, dcp=w.dcp,
@@ -379,6 +380,9 @@ def main():
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="sequences of the headline workload (0: the workload's own); a "
+                         "smaller case for profiler captures, not a bench line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -400,7 +404,7 @@ def main():
     dev = torch.device("cuda", local)
     import decode_context_mla_causal_gb300 as dm
 
-    env = setup(args.config, dev, args.splits)
+    env = setup(args.config, dev, args.splits, args.batch)
     w, dims, step, scale, kvt, ns, flush = (env[k] for k in
                                             ("w", "dims", "step", "scale", "kvt", "ns", "flush"))
     tokens, flops, nbytes = algorithmic(w)
