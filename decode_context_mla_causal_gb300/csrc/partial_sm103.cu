@@ -533,9 +533,16 @@ __device__ __noinline__ void rescale_o(uint32_t tO, float a) {
   tmem_wait_st();
 }
 
-// Stores this warp's rows of the normalised partial output (128 columns).
-__device__ __noinline__ void store_o(uint32_t tO, bool have_o, bool row_ok, float inv,
-                                     float* dst) {
+// Stores this warp's 32 rows of the normalised partial output (its 128 columns),
+// 32 columns at a time: lane r scales row r by its 1/l and writes it into a 4 KB
+// shared-memory slice of this warp (chunk c of row r at 16-byte position c ^ (r mod 8)),
+// then lane l stores chunk (l mod 8) of rows 4k + l/8, k = 0..7, so one instruction
+// writes four whole 128-byte row segments (a store per thread of its own row would
+// touch 32 rows per instruction). Rows at or past rows_left are not written.
+__device__ __noinline__ void store_o(uint32_t tO, bool have_o, int rows_left, float inv,
+                                     float* dst0, uint4* slice) {
+  const int lane = threadIdx.x & 31;
+  const int rsub = lane >> 3, chunk = lane & 7;
   for (int c4 = 0; c4 < 4; ++c4) {
     uint32_t o[32];
     if (have_o) {
@@ -545,56 +552,86 @@ __device__ __noinline__ void store_o(uint32_t tO, bool have_o, bool row_ok, floa
 #pragma unroll
       for (int e = 0; e < 32; ++e) o[e] = 0u;
     }
-    if (row_ok) {
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        float4 v = make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                               __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-        *reinterpret_cast<float4*>(dst + 32 * c4 + e) = v;
-      }
+    for (int c = 0; c < 8; ++c)
+      slice[lane * 8 + (c ^ (lane & 7))] =
+          make_uint4(__float_as_uint(__uint_as_float(o[4 * c]) * inv),
+                     __float_as_uint(__uint_as_float(o[4 * c + 1]) * inv),
+                     __float_as_uint(__uint_as_float(o[4 * c + 2]) * inv),
+                     __float_as_uint(__uint_as_float(o[4 * c + 3]) * inv));
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int row = 4 * k + rsub;
+      if (row < rows_left)
+        *reinterpret_cast<uint4*>(dst0 + (int64_t)row * kDv + 32 * c4 + 4 * chunk) =
+            slice[row * 8 + (chunk ^ (row & 7))];
     }
+    __syncwarp();  // the slice is written again for the next 32 columns
   }
 }
 
-// Q slice of one row into TMEM (16-bit, 2 per column; atom a at columns 32a);
-// half 0 loads atoms 0-2, half 1 the rest. The next atom's 128 bytes are
-// requested before the current one is converted, so the global latency is paid
-// about once. Returns true if some |q| exceeds the f16 range on the FP8 path.
+// Q slices of this warp's 32 rows into TMEM (16-bit, 2 per column; atom a at
+// columns 32a); half 0 loads atoms 0-2, half 1 the rest. Reads are coalesced: for
+// each atom a lane loads 16-byte chunk (lane mod 8) of row 4k + lane/8, k = 0..7, so
+// one instruction covers four whole 128-byte row segments (a load per thread of its
+// own row would touch 32 rows per instruction). The converted chunks go through a
+// 4 KB shared-memory slice of this warp (chunk c of row r at 16-byte position
+// c ^ (r mod 8), conflict-free both ways), from which lane r takes row r for the TMEM
+// store. The next atom's loads are in flight while the current one is converted
+// (requesting every atom at once measured slower: it raises the kernel's register
+// count). Returns true if some |q| exceeds the f16 range on the FP8 path.
 template <bool kFp8, int kAtoms>
-__device__ __noinline__ bool load_q(const uint16_t* src, bool row_ok, int h, uint32_t tQ) {
+__device__ __noinline__ bool load_q(const uint16_t* rows0, int rows_left, int h, uint32_t tQ,
+                                    uint4* slice) {
   bool q_range = false;
+  const int lane = threadIdx.x & 31;
   const int a0 = h == 0 ? 0 : 3;
   const int a1 = h == 0 ? 3 : kAtoms;
+  const int rsub = lane >> 3, chunk = lane & 7;
   uint4 cur[8], nxt[8];
   auto fetch = [&](int a, uint4 (&v)[8]) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-      v[c] = (row_ok && a < a1) ? __ldg(reinterpret_cast<const uint4*>(src + a * 64 + c * 8))
-                                : make_uint4(0u, 0u, 0u, 0u);
+    for (int k = 0; k < 8; ++k) {
+      const int row = 4 * k + rsub;
+      v[k] = (a < a1 && row < rows_left)
+                 ? __ldg(reinterpret_cast<const uint4*>(rows0 + (int64_t)row * kDqk + a * 64 +
+                                                         chunk * 8))
+                 : make_uint4(0u, 0u, 0u, 0u);
+    }
   };
   fetch(a0, cur);
   for (int a = a0; a < a1; ++a) {
     fetch(a + 1, nxt);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      uint4 x = cur[k];
+      if (kFp8) {
+        uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float f0 = __uint_as_float(wv[e] << 16);
+          const float f1 = __uint_as_float(wv[e] & 0xFFFF0000u);
+          q_range |= fabsf(f0) > 65504.f || fabsf(f1) > 65504.f;
+          __half2 hh = __floats2half2_rn(f0, f1);
+          wv[e] = *reinterpret_cast<uint32_t*>(&hh);
+        }
+        x = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      }
+      const int row = 4 * k + rsub;
+      slice[row * 8 + (chunk ^ (row & 7))] = x;
+    }
+    __syncwarp();
     uint32_t w[32];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const uint32_t x[4] = {cur[c].x, cur[c].y, cur[c].z, cur[c].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (kFp8) {
-          const float f0 = __uint_as_float(x[e] << 16);
-          const float f1 = __uint_as_float(x[e] & 0xFFFF0000u);
-          q_range |= fabsf(f0) > 65504.f || fabsf(f1) > 65504.f;
-          __half2 hh = __floats2half2_rn(f0, f1);
-          w[c * 4 + e] = *reinterpret_cast<uint32_t*>(&hh);
-        } else {
-          w[c * 4 + e] = x[e];
-        }
-      }
+      const uint4 x = slice[lane * 8 + (c ^ (lane & 7))];
+      w[4 * c] = x.x, w[4 * c + 1] = x.y, w[4 * c + 2] = x.z, w[4 * c + 3] = x.w;
     }
+    __syncwarp();  // the slice is written again for the next atom
     tmem_st32(tQ + 32 * a, w);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) cur[c] = nxt[c];
+    for (int k = 0; k < 8; ++k) cur[k] = nxt[k];
   }
   tmem_wait_st();
   return q_range;
@@ -657,8 +694,13 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
   const float sc = p.softmax_scale * kv_scale * kLog2e;
 
   {
-    const uint16_t* src = p.q + ((int64_t)it.b * qrows + qr) * kDqk + d0;
-    const bool q_range = load_q<kFp8, kAtoms>(src, row_ok, h, tQ);
+    // this warp's 32 rows start at row qw*32 of the tile; the own-factor buffer, first
+    // written after the first scores (which need every warp's q), lends each warp a
+    // 4 KB slice for the transpose
+    const int r_first = qw * 32;
+    const uint16_t* rows0 = p.q + ((int64_t)it.b * qrows + it.qr0 + r_first) * kDqk + d0;
+    const bool q_range = load_q<kFp8, kAtoms>(rows0, it.rows_valid - r_first, h, tQ,
+                                              sh.eprev + warp * 256);
     tc_fence_before();
     if (q_range) raise_status(p.status, DCP_STATUS_Q_RANGE);
     __syncwarp();
@@ -854,7 +896,12 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
   const int64_t rh = (int64_t)it.b * qrows + qr;
   const int64_t base = ((int64_t)it.k * p.num_splits + it.s) * ((int64_t)R * p.H) + rh;
   const float inv = (paired && l_run > 0.f) ? kv_scale / l_run : 0.f;
-  store_o(tO, have_o, row_ok, inv, p.part_o + base * kDv + 256 * cta + 128 * h);
+  // the warp's first row; every MMA has completed (or none ran), so the KV stages are
+  // free and lend each warp a 4 KB slice for the transpose
+  const int64_t base0 = base - r + qw * 32;
+  store_o(tO, have_o, it.rows_valid - qw * 32, inv,
+          p.part_o + base0 * kDv + 256 * cta + 128 * h,
+          reinterpret_cast<uint4*>(sh.stages) + warp * 256);
   if (row_ok && cta == 0 && h == 0) {
     p.part_m[base] = l_run > 0.f ? M : -INFINITY;
     p.part_l[base] = l_run;
