@@ -362,6 +362,41 @@ def time_steps(env, K, warmup, stream):
                 merge=[ev[i][2].elapsed_time(ev[i][3]) for i in range(K)])
 
 
+def time_packed(env, K, warmup, stream):
+    """One split: the exchange's send buffer made two ways, each timed over K calls
+    after W untimed ones: the partial kernel (fp32 partials) then the pack kernel,
+    and the partial kernel writing the wire format itself (dcp_mla_partial_packed)."""
+    import torch
+
+    import decode_context_mla_causal_gb300 as dm
+
+    w, step, scale = env["w"], env["step"], env["scale"]
+    ex = dm.A2AExchange(step)
+    step.metadata(w.seq_lens, w.block_table)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    for i in range(warmup + K):
+        e = ev[i - warmup] if i >= warmup else None
+        if e:
+            e[0].record(stream)
+        step.partial(w.q, w.kv, scale, w.softmax_scale)
+        if e:
+            e[1].record(stream)
+        ex.pack_ranks(stream)
+        if e:
+            e[2].record(stream)
+        ex.partial_packed(w.q, w.kv, scale, w.softmax_scale, stream)
+        if e:
+            e[3].record(stream)
+    torch.cuda.synchronize()
+    if step.read_status() != 0:
+        raise RuntimeError(f"packed status {step.read_status():#x}")
+    avg = [1e3 * sum(e[j].elapsed_time(e[j + 1]) for e in ev) / K for j in range(3)]
+    return {"partial_us": avg[0], "pack_us": avg[1], "partial_packed_us": avg[2],
+            "saved_us": avg[0] + avg[1] - avg[2],
+            "note": "send buffer of the all-to-all (payload 512): partial + pack, or the "
+                    "partial kernel writing it directly (one split); not part of ms_per_step"}
+
+
 def roofline(flops, nbytes, part_ms, peaks):
     tensor_peak = float(peaks["bf16_tflops"])
     hbm_peak = float(peaks["hbm_gbs"])
@@ -618,6 +653,8 @@ def main():
                                           cby / (cpart / 1e3) / (hp * 1e9)},
                          "l2": ("flushed with a 512 MB write before each timed step"
                                 if e["flush"] is not None else "inputs larger than L2")}
+                if e["ns"] == 1 and cw.num_heads % cw.dcp == 0:
+                    entry["a2a_one_split"] = time_packed(e, K, args.warmup, stream)
                 if not args.no_cpu_baseline:
                     entry["cpu_baseline"], entry["parity"] = cpu_baseline(
                         cw, e["step"].out, e["step"].lse)

@@ -89,6 +89,8 @@ def load() -> ctypes.CDLL:
         "dcp_mla_verify_noalloc": (I, [D, P, P, P, P, I, P, ctypes.c_float, P, P, P, P]),
         "dcp_kv_slot_mapping": (I, [D, P, P, I, I, P, P, P]),
         "dcp_kv_write": (I, [D, P, P, I, P, I, P, P, P]),
+        "dcp_mla_partial_packed": (I, [D, P, P, I, P, ctypes.c_float, I, I, P, P, P, P, P, P, P,
+                                       P]),
         "dcp_a2a_chunk_words": (ctypes.c_int64, [D, I]),
         "dcp_a2a_pack": (I, [D, I, P, P, P, P, P, P]),
         "dcp_a2a_project": (I, [D, I, P, P, I, P, P, P]),
@@ -202,6 +204,34 @@ def dcp_mla_partial(dims, q, kv, kv_dtype, kv_scale, softmax_scale, rank_begin, 
         _ptr(part_o, f32, num_ranks * NS * R * H * V_DIM, "part_o"),
         _ptr(part_m, f32, num_ranks * NS * R * H, "part_m"),
         _ptr(part_l, f32, num_ranks * NS * R * H, "part_l"),
+        _ptr(workspace, None, None, "workspace", allow_none=True),
+        _ptr(status, i32, 1, "status"), _stream(stream)))
+
+
+def dcp_mla_partial_packed(dims, q, kv, kv_dtype, kv_scale, softmax_scale, rank_begin,
+                           num_ranks, row_len, page_ids, split_beg, split_end, send, status,
+                           stream=None, workspace=None):
+    """Partial attention of ranks ``rank_begin ..`` with one split, each rank's BF16
+    output and LSE written straight into ``send`` (the all-to-all wire format, payload
+    512) instead of fp32 partials."""
+    lib = load()
+    B, R, H = dims.batch, dims.rows, dims.num_heads
+    MP = lib.dcp_mla_max_pages(ctypes.byref(dims))
+    i32 = torch.int32
+    f32 = torch.float32
+    kv_elem = torch.uint8 if kv_dtype == KV_FP8_E4M3 else torch.bfloat16
+    pool = dims.num_blocks * dims.block_size * QK_DIM
+    cw = lib.dcp_a2a_chunk_words(ctypes.byref(dims), V_DIM)
+    _check(lib.dcp_mla_partial_packed(
+        ctypes.byref(dims), _ptr(q, torch.bfloat16, R * H * QK_DIM, "q"),
+        _ptr(kv, kv_elem, num_ranks * pool, "kv"), int(kv_dtype),
+        _ptr(kv_scale, f32, 1, "kv_scale", allow_none=True), float(softmax_scale),
+        rank_begin, num_ranks,
+        _ptr(row_len, i32, num_ranks * R, "row_len"),
+        _ptr(page_ids, i32, num_ranks * B * max(MP, 0), "page_ids"),
+        _ptr(split_beg, i32, num_ranks * B, "split_beg"),
+        _ptr(split_end, i32, num_ranks * B, "split_end"),
+        _ptr(send, torch.bfloat16, num_ranks * dims.dcp * max(cw, 0), "send"),
         _ptr(workspace, None, None, "workspace", allow_none=True),
         _ptr(status, i32, 1, "status"), _stream(stream)))
 

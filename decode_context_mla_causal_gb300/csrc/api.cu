@@ -138,6 +138,38 @@ dcp_status dcp_mla_partial(const dcp_mla_dims* dims, const void* q, const void* 
                   "dcp_mla_partial");
 }
 
+dcp_status dcp_mla_partial_packed(const dcp_mla_dims* dims, const void* q, const void* kv,
+                                  dcp_kv_dtype kv_dtype, const float* kv_scale,
+                                  float softmax_scale, int32_t rank_begin, int32_t num_ranks,
+                                  const int32_t* row_len, const int32_t* page_ids,
+                                  const int32_t* split_beg, const int32_t* split_end,
+                                  void* send, void* workspace, uint32_t* status,
+                                  dcp_stream_t stream) {
+  dcp_status s = check(dims, rank_begin, num_ranks);
+  if (s != DCP_OK) return s;
+  if (dims->num_splits != 1)
+    return fail(DCP_ERR_UNSUPPORTED, "dcp_mla_partial_packed needs num_splits == 1 (got %d)",
+                dims->num_splits);
+  if (dims->num_heads % dims->dcp != 0)
+    return fail(DCP_ERR_UNSUPPORTED, "num_heads (%d) must be a multiple of dcp (%d)",
+                dims->num_heads, dims->dcp);
+  if (kv_dtype != DCP_KV_BF16 && kv_dtype != DCP_KV_FP8_E4M3)
+    return fail(DCP_ERR_INVALID_ARG, "unknown kv_dtype %d", (int)kv_dtype);
+  if (!(softmax_scale > 0.0f) || softmax_scale > 1e30f)
+    return fail(DCP_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+  if (dims->batch == 0) return DCP_OK;
+  if (!q || !kv || !row_len || !page_ids || !split_beg || !split_end || !send || !status)
+    return fail(DCP_ERR_INVALID_ARG, "dcp_mla_partial_packed: a required pointer is NULL");
+  if (((uintptr_t)q & 15) || ((uintptr_t)kv & 15) || ((uintptr_t)send & 15) ||
+      ((uintptr_t)workspace & 15))
+    return fail(DCP_ERR_INVALID_ARG, "q, kv, send and workspace must be 16-byte aligned");
+  Derived x = derive(*dims);
+  return launched(launch_partial(*dims, x, q, kv, kv_dtype, kv_scale, softmax_scale, num_ranks,
+                                 row_len, page_ids, split_beg, split_end, nullptr, nullptr,
+                                 nullptr, workspace, status, (cudaStream_t)stream, send),
+                  "dcp_mla_partial_packed");
+}
+
 dcp_status dcp_mla_workspace_size(const dcp_mla_dims* dims, int32_t num_ranks, size_t* bytes) {
   dcp_status s = check(dims, 0, num_ranks);
   if (s != DCP_OK) return s;

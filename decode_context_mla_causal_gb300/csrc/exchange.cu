@@ -59,6 +59,35 @@ a2a_pack_kernel(int R, int H, int G, int num_splits, int64_t cw, const float* __
   const int Hg = H / G, d = h / Hg, hl = h % Hg;
   const int64_t p0 = (int64_t)k * num_splits * rows_heads + rh;  // split 0 of this rank
   const int dim = threadIdx.x * 4;
+  uint16_t* chunk = send + ((int64_t)k * G + d) * cw;
+  if (rh == 0) {  // the zero words that end each of this rank's chunks
+    const int64_t used = (int64_t)R * Hg * (kDv + 2);
+    for (int dd = 0; dd < G; ++dd)
+      for (int64_t w = used + threadIdx.x; w < cw; w += blockDim.x)
+        send[((int64_t)k * G + dd) * cw + w] = 0;
+  }
+  if (num_splits == 1) {
+    // one split: its normalised output as it is, LSE = (m + log2 l) ln 2 (the same
+    // arithmetic as the partial kernel's packed epilogue, so both give the same bits)
+    const float m = part_m[p0], l = part_l[p0];
+    const bool live = m != -INFINITY && l > 0.f;
+    const float4 o = live ? *reinterpret_cast<const float4*>(part_o + p0 * kDv + dim)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(o.z, o.w);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&lo);
+    v.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(chunk + ((int64_t)row * Hg + hl) * kDv + dim) = v;
+    if (threadIdx.x == 0) {
+      const float lse = live ? (m + log2f(l)) * kLn2 : -INFINITY;
+      const uint32_t bits = __float_as_uint(lse);
+      uint16_t* lp = chunk + (int64_t)R * Hg * kDv + ((int64_t)row * Hg + hl) * 2;
+      lp[0] = (uint16_t)(bits & 0xFFFFu);
+      lp[1] = (uint16_t)(bits >> 16);
+    }
+    return;
+  }
   // one pass with a running maximum: each batch's m, l and o loads are in flight
   // together, the sums rescaled by 2^(M_old - M_new) when M rises
   float M = -INFINITY;
@@ -107,7 +136,6 @@ a2a_pack_kernel(int R, int H, int G, int num_splits, int64_t cw, const float* __
     }
   }
   const float inv = den > 0.f ? 1.0f / den : 0.f;
-  uint16_t* chunk = send + ((int64_t)k * G + d) * cw;
   __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
   __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
   uint2 v;
@@ -120,12 +148,6 @@ a2a_pack_kernel(int R, int H, int G, int num_splits, int64_t cw, const float* __
     uint16_t* lp = chunk + (int64_t)R * Hg * kDv + ((int64_t)row * Hg + hl) * 2;
     lp[0] = (uint16_t)(bits & 0xFFFFu);
     lp[1] = (uint16_t)(bits >> 16);
-  }
-  if (rh == 0) {  // the zero words that end each of this rank's chunks
-    const int64_t used = (int64_t)R * Hg * (kDv + 2);
-    for (int dd = 0; dd < G; ++dd)
-      for (int64_t w = used + threadIdx.x; w < cw; w += blockDim.x)
-        send[((int64_t)k * G + dd) * cw + w] = 0;
   }
 }
 

@@ -157,6 +157,11 @@ struct Params {
   float* part_l;
   uint32_t* status;
   const int32_t* item_order;  // cluster -> work item (longest first), or null: natural order
+  // packed epilogue (one split): the all-to-all send buffers [rank][G][cw words] get the
+  // BF16 output and the LSE words instead of part_o/m/l (null: the fp32 partials)
+  uint16_t* send;
+  int64_t send_cw;
+  int G;
   float softmax_scale;
   int batch, qlen, H, num_splits, subpage, max_pages, n_row_tiles;
   int64_t pool_rows;  // rows of one rank's pool: num_blocks * block_size
@@ -571,6 +576,63 @@ __device__ __noinline__ void store_o(uint32_t tO, bool have_o, int rows_left, fl
   }
 }
 
+// The packed epilogue: this warp's 32 rows of its 128 output columns, normalised
+// and rounded to BF16 (nearest even), written into the all-to-all send buffer: query
+// row qr of the tile is head qr mod H of verify row qr / H, whose entry lives in the
+// chunk for the head's destination. 64 columns at a time go through the warp's 4 KB
+// slice (as in store_o), so one instruction stores four 128-byte row segments.
+// send_k: this rank's send buffer; cw: words per chunk; qr_first: the warp's first
+// query row; entry_row0: verify-row index of the sequence's first row (b * qlen);
+// col0: the first of the warp's output columns.
+__device__ __noinline__ void store_o_packed(uint32_t tO, bool have_o, int rows_left, float inv,
+                                            uint4* slice, uint16_t* send_k, int64_t cw, int H,
+                                            int Hg, int qr_first, int64_t entry_row0, int col0) {
+  const int lane = threadIdx.x & 31;
+  const int rsub = lane >> 3, chunk = lane & 7;
+  uint16_t* dst[8];  // the send-buffer entry of each row this lane stores
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int qrk = qr_first + 4 * k + rsub;
+    const int jk = qrk / H, hk = qrk - jk * H;
+    const int dk = hk / Hg;
+    dst[k] = send_k + dk * cw + ((entry_row0 + jk) * Hg + (hk - dk * Hg)) * kDv + col0;
+  }
+  for (int c8 = 0; c8 < 2; ++c8) {
+    uint32_t o[64];
+    if (have_o) {
+      uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[0]);
+      uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[32]);
+      tmem_ld32(tO + 64 * c8, o0);
+      tmem_ld32(tO + 64 * c8 + 32, o1);
+      tmem_wait_ld(o0);
+      tmem_wait_ld(o1);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 64; ++e) o[e] = 0u;
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[8 * c + 2 * e]) * inv,
+                                                  __uint_as_float(o[8 * c + 2 * e + 1]) * inv);
+        w[e] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      slice[lane * 8 + (c ^ (lane & 7))] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int row = 4 * k + rsub;
+      if (row < rows_left)
+        *reinterpret_cast<uint4*>(dst[k] + 64 * c8 + 8 * chunk) =
+            slice[row * 8 + (chunk ^ (row & 7))];
+    }
+    __syncwarp();  // the slice is written again for the next 64 columns
+  }
+}
+
 // Q slices of this warp's 32 rows into TMEM (16-bit, 2 per column; atom a at
 // columns 32a); half 0 loads atoms 0-2, half 1 the rest. Reads are coalesced: for
 // each atom a lane loads 16-byte chunk (lane mod 8) of row 4k + lane/8, k = 0..7, so
@@ -898,10 +960,34 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
   const float inv = (paired && l_run > 0.f) ? kv_scale / l_run : 0.f;
   // the warp's first row; every MMA has completed (or none ran), so the KV stages are
   // free and lend each warp a 4 KB slice for the transpose
+  uint4* slice = reinterpret_cast<uint4*>(sh.stages) + warp * 256;
+  if (p.send != nullptr) {
+    // packed epilogue
+    const int Hg = p.H / p.G;
+    store_o_packed(tO, have_o, it.rows_valid - qw * 32, inv, slice,
+                   p.send + (int64_t)it.k * p.G * p.send_cw, p.send_cw, p.H, Hg,
+                   it.qr0 + qw * 32, (int64_t)it.b * p.qlen, 256 * cta + 128 * h);
+    if (row_ok && cta == 0 && h == 0) {
+      // the LSE words (low 16 bits, then high), as one 32-bit store
+      const float lse = l_run > 0.f ? (M + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      const int hh = qr - j * p.H, dd = hh / Hg;
+      const int64_t entry = ((int64_t)it.b * p.qlen + j) * Hg + (hh - dd * Hg);
+      uint16_t* cbase = p.send + ((int64_t)it.k * p.G + dd) * p.send_cw;
+      *reinterpret_cast<uint32_t*>(cbase + (int64_t)R * Hg * kDv + entry * 2) =
+          __float_as_uint(lse);
+    }
+    if (cta == 0 && it.b == 0 && it.t == 0 && tid == 0) {
+      // the zero words that end each of this rank's chunks
+      const int64_t used = (int64_t)R * Hg * (kDv + 2);
+      for (int dd = 0; dd < p.G; ++dd)
+        for (int64_t w = used; w < p.send_cw; ++w)
+          p.send[((int64_t)it.k * p.G + dd) * p.send_cw + w] = 0;
+    }
+    return;
+  }
   const int64_t base0 = base - r + qw * 32;
-  store_o(tO, have_o, it.rows_valid - qw * 32, inv,
-          p.part_o + base0 * kDv + 256 * cta + 128 * h,
-          reinterpret_cast<uint4*>(sh.stages) + warp * 256);
+  store_o(tO, have_o, it.rows_valid - qw * 32, inv, p.part_o + base0 * kDv + 256 * cta + 128 * h,
+          slice);
   if (row_ok && cta == 0 && h == 0) {
     p.part_m[base] = l_run > 0.f ? M : -INFINITY;
     p.part_l[base] = l_run;
@@ -1056,7 +1142,7 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
                            const int32_t* page_ids, const int32_t* split_beg,
                            const int32_t* split_end, float* part_o, float* part_m,
                            float* part_l, void* workspace, uint32_t* status,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, void* send) {
   Params p;
   p.q = reinterpret_cast<const uint16_t*>(q);
   p.kv = reinterpret_cast<const uint8_t*>(kv);
@@ -1070,6 +1156,9 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
   p.part_l = part_l;
   p.status = status;
   p.item_order = nullptr;
+  p.send = reinterpret_cast<uint16_t*>(send);
+  p.G = d.dcp;
+  p.send_cw = send ? a2a_chunk_words(d.batch * d.qlen, d.num_heads / d.dcp, kDv) : 0;
   p.softmax_scale = softmax_scale;
   p.batch = d.batch;
   p.qlen = d.qlen;

@@ -55,6 +55,16 @@ class A2AExchange:
         if self.w_v is not None:
             self.project(stream)
 
+    def partial_packed(self, q, kv, kv_scale, softmax_scale, stream=None):
+        """One split: the step's partial attention writing each rank's BF16 output and
+        LSE straight into the send buffer (payload 512; the step's fp32 partials are
+        not written), in place of ``step.partial`` followed by ``pack_ranks``."""
+        s = self.step
+        B.dcp_mla_partial_packed(s.dims, q, kv, s.kv_dtype, kv_scale, softmax_scale,
+                                 s.rank_begin, s.num_ranks, s.row_len, s.page_ids, s.split_beg,
+                                 s.split_end, self.packed, s.status, stream,
+                                 workspace=s.workspace)
+
     def pack_ranks(self, stream=None):
         """Each rank's merged BF16 output and LSE (payload 512)."""
         s = self.step

@@ -330,6 +330,31 @@ dcp_status dcp_kv_write(const dcp_mla_dims* dims, const int32_t* slot_mapping, c
  *   status      never written (no data-dependent failure, no wait); may be NULL
  */
 int64_t dcp_a2a_chunk_words(const dcp_mla_dims* dims, int32_t payload);
+
+/*
+ * Step 3 and the pack of the exchange in one call, for one split: the partial
+ * attention of dcp_mla_partial, with each rank's normalised output rounded to BF16
+ * (nearest even) and its natural-log LSE written straight into its all-to-all send
+ * buffer, in the wire format of dcp_a2a_pack (P = 512), instead of the fp32 partials.
+ * Defined by: "[ROCm][MLA][DCP] Support causal multi-token verification",
+ * Implementation item 3 (each rank's partial output and LSE) and "Context Parallel
+ * Guide (PCP & DCP)", comm_backend a2a (the output travels as BF16 with the fp32 LSE
+ * in two 16-bit halves); a rank with one split has nothing to merge before it sends.
+ *
+ *   dims->num_splits must be 1 and num_heads a multiple of dcp (else
+ *   DCP_ERR_UNSUPPORTED); the other arguments as for dcp_mla_partial
+ *   send      device, 16-byte aligned, [num_ranks][dcp][dcp_a2a_chunk_words(dims,
+ *             512)] 16-bit words, out: the same bits dcp_mla_partial followed by
+ *             dcp_a2a_pack would write (a one-split LSE is (m + log2 l) ln 2)
+ *   status    device uint32 [1], in/out: as for dcp_mla_partial
+ */
+dcp_status dcp_mla_partial_packed(const dcp_mla_dims* dims, const void* q, const void* kv,
+                                  dcp_kv_dtype kv_dtype, const float* kv_scale,
+                                  float softmax_scale, int32_t rank_begin, int32_t num_ranks,
+                                  const int32_t* row_len, const int32_t* page_ids,
+                                  const int32_t* split_beg, const int32_t* split_end,
+                                  void* send, void* workspace, uint32_t* status,
+                                  dcp_stream_t stream);
 dcp_status dcp_a2a_pack(const dcp_mla_dims* dims, int32_t num_ranks, const float* part_o,
                         const float* part_m, const float* part_l, void* send, uint32_t* status,
                         dcp_stream_t stream);

@@ -206,3 +206,49 @@ def test_graph_capture_of_step_and_exchange(dm):
         assert torch.equal(got[0].view(torch.int16), fex.out.view(torch.int16))
         assert torch.equal(got[1], fex.lse)
         assert torch.equal(got[2].view(torch.int16), fex.send.view(torch.int16))
+
+
+# One split: the partial kernel writes the wire format itself (dcp_mla_partial_packed).
+# Its send buffer must hold the very bits of dcp_mla_partial followed by dcp_a2a_pack,
+# the zero words at the end of every chunk included; the combine of it then passes the
+# oracle checks above (test_a2a_*), so it is compared bit for bit here.
+PACKED = [
+    ("c1", None),
+    ("c2", dict(batch=3, num_heads=96, qlen=3, dcp=2, interleave=2, block_size=64,
+                kv_dtype="fp8", max_local_len=700, lengths=("uniform", 3, 1300))),
+    ("c2", dict(batch=2, num_heads=128, qlen=5, dcp=8, interleave=64, block_size=64,
+                kv_dtype="fp8", max_local_len=1024, lengths=("uniform", 5, 6000))),
+    ("c2", dict(batch=2, num_heads=16, qlen=2, dcp=4, interleave=1, block_size=96,
+                kv_dtype="bf16", max_local_len=400, lengths=("uniform", 2, 1100))),
+    ("c3", None),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(PACKED)))
+def test_partial_packed_equals_partial_then_pack(dm, idx):
+    name, ov = PACKED[idx]
+    w = workloads.generate(name, device="cuda", seed_index=None if ov is None else 90 + idx,
+                           overrides=ov)
+    step = dm.VerifyStep(h.dims_of(dm, w, 1), h.kv_dtype_of(dm, w), "cuda")
+    scale = torch.tensor([w.kv_scale], dtype=torch.float32, device="cuda")
+    step.metadata(w.seq_lens, w.block_table)
+    step.partial(w.q, w.kv, scale, w.softmax_scale)
+    ex = dm.A2AExchange(step)
+    ex.pack_ranks()
+    torch.cuda.synchronize()
+    want = ex.send.clone()
+    ex.send.fill_(float("nan"))  # every word must be written again
+    ex.partial_packed(w.q, w.kv, scale, w.softmax_scale)
+    torch.cuda.synchronize()
+    assert step.read_status() == 0
+    assert torch.equal(ex.send.view(torch.int16), want.view(torch.int16))
+
+
+def test_partial_packed_rejects_more_than_one_split(dm):
+    w = workloads.generate("c1", device="cuda")
+    step = dm.VerifyStep(h.dims_of(dm, w, 2), h.kv_dtype_of(dm, w), "cuda")
+    ex = dm.A2AExchange(step)
+    scale = torch.tensor([w.kv_scale], dtype=torch.float32, device="cuda")
+    with pytest.raises(dm.DcpError) as ei:
+        ex.partial_packed(w.q, w.kv, scale, w.softmax_scale)
+    assert ei.value.code == dm.DCP_ERR_UNSUPPORTED
