@@ -397,6 +397,64 @@ def time_packed(env, K, warmup, stream):
                     "partial kernel writing it directly (one split); not part of ms_per_step"}
 
 
+def time_a2a(env, K, warmup, stream):
+    """The step after the path: each rank's result in the all-to-all wire format
+    (pack), then the combine with every rank on this device; plain (512 latent dims
+    per head) and with project-before-merge (synthetic W_V, 512 -> 128). Each kernel
+    timed over K rounds after W untimed ones, with its HBM bytes per launch."""
+    import torch
+
+    import decode_context_mla_causal_gb300 as dm
+    import workloads
+
+    w, step, ns = env["w"], env["step"], env["ns"]
+    if w.num_heads % w.dcp != 0:
+        return None
+    dev = w.q.device
+    a2a = {}
+    w_v = workloads.generate_w_v(w.num_heads, 128, device=dev)
+    nr, R, H = w.dcp, w.rows, w.num_heads
+    for label, wv in (("plain", None), ("project_before_merge", w_v)):
+        ex = dm.A2AExchange(step, w_v=wv)
+        a_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+        for i in range(warmup + K):
+            e = a_ev[i - warmup] if i >= warmup else None
+            if e:
+                e[0].record(stream)
+            ex.pack_ranks(stream)
+            if e:
+                e[1].record(stream)
+            if wv is not None:
+                ex.project(stream)
+            if e:
+                e[2].record(stream)
+            ex.combine_local(stream)
+            if e:
+                e[3].record(stream)
+        torch.cuda.synchronize()
+        if step.read_status() != 0:
+            raise RuntimeError(f"a2a status {step.read_status():#x}")
+        avg = [1e3 * sum(e[j].elapsed_time(e[j + 1]) for e in a_ev) / K for j in range(3)]
+        packed_bytes = ex.packed.numel() * 2
+        send_bytes = ex.send.numel() * 2
+        pack_bytes = nr * ns * R * H * (4 * 512 + 8) + packed_bytes
+        comb_bytes = send_bytes + R * H * (2 * ex.payload + 4)
+        a2a[label] = {"payload": ex.payload, "send_bytes": send_bytes,
+                      "kernel_us": {"pack": avg[0], "combine": avg[2]},
+                      "pack_hbm_gbs": pack_bytes / (avg[0] / 1e6) / 1e9,
+                      "combine_hbm_gbs": comb_bytes / (avg[2] / 1e6) / 1e9}
+        if wv is not None:
+            a2a[label]["kernel_us"]["project"] = avg[1]
+            a2a[label]["project_tflops"] = 2.0 * nr * R * H * 512 * ex.payload / (avg[1] / 1e6) / 1e12
+            a2a[label]["project_hbm_gbs"] = (
+                packed_bytes + wv.numel() * 2 + send_bytes) / (avg[1] / 1e6) / 1e9
+        del ex
+    a2a["note"] = ("all-to-all wire format (BF16 output + float32 LSE as two 16-bit "
+                   "halves), combined on this device; timed separately, not part of "
+                   "ms_per_step")
+    return a2a
+
+
 def roofline(flops, nbytes, part_ms, peaks):
     tensor_peak = float(peaks["bf16_tflops"])
     hbm_peak = float(peaks["hbm_gbs"])
@@ -531,52 +589,7 @@ def main():
     kv_map_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in kw_ev) / K
     kv_write_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in kw_ev) / K
 
-    # the step after the path: each rank's result in the all-to-all wire format
-    # (pack), then the combine with every rank on this device; plain (512 latent
-    # dims per head) and with project-before-merge (synthetic W_V, 512 -> 128)
-    a2a = None
-    if w.num_heads % w.dcp == 0:
-        a2a = {}
-        w_v = workloads.generate_w_v(w.num_heads, 128, device=dev)
-        nr, R, H = w.dcp, w.rows, w.num_heads
-        for label, wv in (("plain", None), ("project_before_merge", w_v)):
-            ex = dm.A2AExchange(step, w_v=wv)
-            a_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-            for i in range(args.warmup + K):
-                e = a_ev[i - args.warmup] if i >= args.warmup else None
-                if e:
-                    e[0].record(stream)
-                ex.pack_ranks(stream)
-                if e:
-                    e[1].record(stream)
-                if wv is not None:
-                    ex.project(stream)
-                if e:
-                    e[2].record(stream)
-                ex.combine_local(stream)
-                if e:
-                    e[3].record(stream)
-            torch.cuda.synchronize()
-            if step.read_status() != 0:
-                raise RuntimeError(f"a2a status {step.read_status():#x}")
-            avg = [1e3 * sum(e[j].elapsed_time(e[j + 1]) for e in a_ev) / K for j in range(3)]
-            packed_bytes = ex.packed.numel() * 2
-            send_bytes = ex.send.numel() * 2
-            pack_bytes = nr * ns * R * H * (4 * 512 + 8) + packed_bytes
-            comb_bytes = send_bytes + R * H * (2 * ex.payload + 4)
-            a2a[label] = {"payload": ex.payload, "send_bytes": send_bytes,
-                          "kernel_us": {"pack": avg[0], "combine": avg[2]},
-                          "pack_hbm_gbs": pack_bytes / (avg[0] / 1e6) / 1e9,
-                          "combine_hbm_gbs": comb_bytes / (avg[2] / 1e6) / 1e9}
-            if wv is not None:
-                a2a[label]["kernel_us"]["project"] = avg[1]
-                a2a[label]["project_tflops"] = 2.0 * nr * R * H * 512 * ex.payload / (avg[1] / 1e6) / 1e12
-                a2a[label]["project_hbm_gbs"] = (
-                    packed_bytes + wv.numel() * 2 + send_bytes) / (avg[1] / 1e6) / 1e9
-            del ex
-        a2a["note"] = ("all-to-all wire format (BF16 output + float32 LSE as two 16-bit "
-                       "halves), combined on this device; timed separately, not part of "
-                       "ms_per_step")
+    a2a = time_a2a(env, K, args.warmup, stream)
 
     peaks, src = load_peaks()
     part_avg = sum(part_ms) / K
@@ -653,6 +666,8 @@ def main():
                                           cby / (cpart / 1e3) / (hp * 1e9)},
                          "l2": ("flushed with a 512 MB write before each timed step"
                                 if e["flush"] is not None else "inputs larger than L2")}
+                if cfg in ("c3", "c4"):  # the exchange at the sizes where HBM rate means something
+                    entry["a2a"] = time_a2a(e, K, args.warmup, stream)
                 if e["ns"] == 1 and cw.num_heads % cw.dcp == 0:
                     entry["a2a_one_split"] = time_packed(e, K, args.warmup, stream)
                 if not args.no_cpu_baseline:

@@ -11,13 +11,13 @@
 // halves (low 16 bits, then high 16 bits of the float32), then zero words up to a
 // multiple of 8 words. A source's send buffer is [dcp][chunk].
 //
-//   a2a_pack_kernel     one CTA per (row, head, rank): merges the rank's splits
-//                       (m, l, o) into its normalised output, RNE to BF16, and its
-//                       natural-log LSE, written into the chunk for the head's
-//                       destination. HBM-bound: reads NS*(2 KiB + 8 B), writes
-//                       1 KiB + 4 B per (rank, row, head).
-//   a2a_combine_kernel  one CTA per (destination, row, head of its slice): reads the
-//                       dcp source entries, LSE-weights them. HBM-bound: reads
+//   a2a_pack_kernel     one warp per (rank, row, head), grid-stride: merges the
+//                       rank's splits (m, l, o) into its normalised output, RNE to
+//                       BF16, and its natural-log LSE, written into the chunk for
+//                       the head's destination. HBM-bound: reads NS*(2 KiB + 8 B),
+//                       writes 1 KiB + 4 B per (rank, row, head).
+//   a2a_combine_kernel  one warp per (destination, row, head of its slice): reads
+//                       the dcp source entries, LSE-weights them. HBM-bound: reads
 //                       dcp*(2P + 4) B, writes 2P + 4 B per (row, head).
 //
 // Project-before-merge ("enable_project_before_merge" on the same page): each
@@ -37,6 +37,8 @@
 //                       copied.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "sm103.cuh"
 
@@ -47,179 +49,266 @@ using namespace sm103;
 
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int kBatch>  // splits whose loads are in flight together (1 when there is one)
-__global__ void __launch_bounds__(128)
-a2a_pack_kernel(int R, int H, int G, int num_splits, int64_t cw, const float* __restrict__ part_o,
-                const float* __restrict__ part_m, const float* __restrict__ part_l,
-                uint16_t* __restrict__ send) {
+constexpr int kXWarps = 8;  // warps (entries in flight) per CTA of pack and combine
+
+// 8 floats, each times scale, as 8 BF16 values (one 16-byte chunk)
+__device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8], float scale) {
+  uint32_t w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(f[2 * e] * scale, f[2 * e + 1] * scale);
+    w[e] = *reinterpret_cast<uint32_t*>(&t);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One warp per (rank, row, head) entry, grid-stride: lane l owns dims [16l, 16l + 16).
+// More than one split: one pass with a running maximum over the splits' m, four
+// splits' loads in flight together, the sums rescaled by 2^(M_old - M_new) when M
+// rises. One split: its normalised output as it is and LSE = (m + log2 l) ln 2 (the
+// same arithmetic as the partial kernel's packed epilogue, so both give the same bits).
+template <bool kOne>  // one split: no merge, fewer registers, more warps resident
+__global__ void __launch_bounds__(32 * kXWarps, kOne ? 4 : 2)
+a2a_pack_kernel(int R, int H, int G, int num_splits, int num_ranks, int64_t cw,
+                const float* __restrict__ part_o, const float* __restrict__ part_m,
+                const float* __restrict__ part_l, uint16_t* __restrict__ send) {
   const int rows_heads = R * H;
-  const int rh = blockIdx.x;
-  const int k = blockIdx.y;  // rank within the call
-  const int row = rh / H, h = rh % H;
-  const int Hg = H / G, d = h / Hg, hl = h % Hg;
-  const int64_t p0 = (int64_t)k * num_splits * rows_heads + rh;  // split 0 of this rank
-  const int dim = threadIdx.x * 4;
-  uint16_t* chunk = send + ((int64_t)k * G + d) * cw;
-  if (rh == 0) {  // the zero words that end each of this rank's chunks
-    const int64_t used = (int64_t)R * Hg * (kDv + 2);
-    for (int dd = 0; dd < G; ++dd)
-      for (int64_t w = used + threadIdx.x; w < cw; w += blockDim.x)
-        send[((int64_t)k * G + dd) * cw + w] = 0;
-  }
-  if (num_splits == 1) {
-    // one split: its normalised output as it is, LSE = (m + log2 l) ln 2 (the same
-    // arithmetic as the partial kernel's packed epilogue, so both give the same bits)
-    const float m = part_m[p0], l = part_l[p0];
-    const bool live = m != -INFINITY && l > 0.f;
-    const float4 o = live ? *reinterpret_cast<const float4*>(part_o + p0 * kDv + dim)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-    __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(o.z, o.w);
-    uint2 v;
-    v.x = *reinterpret_cast<uint32_t*>(&lo);
-    v.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(chunk + ((int64_t)row * Hg + hl) * kDv + dim) = v;
-    if (threadIdx.x == 0) {
-      const float lse = live ? (m + log2f(l)) * kLn2 : -INFINITY;
-      const uint32_t bits = __float_as_uint(lse);
-      uint16_t* lp = chunk + (int64_t)R * Hg * kDv + ((int64_t)row * Hg + hl) * 2;
-      lp[0] = (uint16_t)(bits & 0xFFFFu);
-      lp[1] = (uint16_t)(bits >> 16);
+  const int Hg = H / G;
+  const int lane = threadIdx.x & 31;
+  const int64_t n_entries = (int64_t)num_ranks * rows_heads;
+  const int64_t stride = (int64_t)gridDim.x * kXWarps;
+  for (int64_t e = (int64_t)blockIdx.x * kXWarps + (threadIdx.x >> 5); e < n_entries;
+       e += stride) {
+    const int k = (int)(e / rows_heads);
+    const int rh = (int)(e - (int64_t)k * rows_heads);
+    const int row = rh / H, h = rh - row * H;
+    const int d = h / Hg, hl = h - d * Hg;
+    const int64_t p0 = (int64_t)k * num_splits * rows_heads + rh;  // split 0 of this rank
+    uint16_t* chunk = send + ((int64_t)k * G + d) * cw;
+    if (rh == 0) {  // the zero words that end each of this rank's chunks
+      const int64_t used = (int64_t)R * Hg * (kDv + 2);
+      for (int dd = 0; dd < G; ++dd)
+        for (int64_t w = used + lane; w < cw; w += 32) send[((int64_t)k * G + dd) * cw + w] = 0;
     }
-    return;
-  }
-  // one pass with a running maximum: each batch's m, l and o loads are in flight
-  // together, the sums rescaled by 2^(M_old - M_new) when M rises
-  float M = -INFINITY;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
-  for (int s0 = 0; s0 < num_splits; s0 += kBatch) {
-    float m[kBatch], l[kBatch];
-    float4 o[kBatch];
+    float M = -INFINITY, den = 0.f;
+    float acc[16];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      m[u] = -INFINITY;
-      l[u] = 0.f;
-      o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (s0 + u < num_splits) {  // no load at all past the last split
-        const int64_t i = p0 + (int64_t)(s0 + u) * rows_heads;
-        m[u] = part_m[i];
-        l[u] = part_l[i];
-        o[u] = *reinterpret_cast<const float4*>(part_o + i * kDv + dim);
+    for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+    float lse;
+    if (kOne) {
+      // the output's loads do not wait for m and l: a dead entry's values are dropped
+      const float4* src = reinterpret_cast<const float4*>(part_o + p0 * kDv + 16 * lane);
+      float4 v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] = src[q];
+      const float m = part_m[p0], l = part_l[p0];
+      const bool live = m != -INFINITY && l > 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[4 * q] = live ? v[q].x : 0.f;
+        acc[4 * q + 1] = live ? v[q].y : 0.f;
+        acc[4 * q + 2] = live ? v[q].z : 0.f;
+        acc[4 * q + 3] = live ? v[q].w : 0.f;
       }
-    }
-    float Mb = M;
+      den = live ? 1.f : 0.f;
+      lse = live ? (m + log2f(l)) * kLn2 : -INFINITY;
+    } else {
+      for (int s0 = 0; s0 < num_splits; s0 += 4) {
+        float m[4], l[4];
+        float4 o[4][4];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      if (!(s0 + u < num_splits && m[u] != -INFINITY && l[u] > 0.f)) m[u] = -INFINITY;
-      Mb = fmaxf(Mb, m[u]);
-    }
-    if (Mb == -INFINITY) continue;
-    if (Mb != M) {
-      const float a = M == -INFINITY ? 0.f : exp2f(M - Mb);
-      den *= a;
-      acc.x *= a;
-      acc.y *= a;
-      acc.z *= a;
-      acc.w *= a;
-      M = Mb;
-    }
+        for (int u = 0; u < 4; ++u) {
+          m[u] = -INFINITY;
+          l[u] = 0.f;
+          if (s0 + u < num_splits) {  // no load at all past the last split
+            const int64_t i = p0 + (int64_t)(s0 + u) * rows_heads;
+            m[u] = part_m[i];
+            l[u] = part_l[i];
+            const float4* src = reinterpret_cast<const float4*>(part_o + i * kDv + 16 * lane);
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const float w = m[u] == -INFINITY ? 0.f : exp2f(m[u] - M) * l[u];
-      const float4 ov = m[u] == -INFINITY ? make_float4(0.f, 0.f, 0.f, 0.f) : o[u];
-      den += w;
-      acc.x = fmaf(w, ov.x, acc.x);
-      acc.y = fmaf(w, ov.y, acc.y);
-      acc.z = fmaf(w, ov.z, acc.z);
-      acc.w = fmaf(w, ov.w, acc.w);
+            for (int q = 0; q < 4; ++q) o[u][q] = src[q];
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o[u][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+        float Mb = M;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (!(m[u] != -INFINITY && l[u] > 0.f)) m[u] = -INFINITY;
+          Mb = fmaxf(Mb, m[u]);
+        }
+        if (Mb == -INFINITY) continue;
+        if (Mb != M) {
+          const float a = M == -INFINITY ? 0.f : exp2f(M - Mb);
+          den *= a;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) acc[c] *= a;
+          M = Mb;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (m[u] == -INFINITY) continue;
+          const float w = exp2f(m[u] - M) * l[u];
+          den += w;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[4 * q] = fmaf(w, o[u][q].x, acc[4 * q]);
+            acc[4 * q + 1] = fmaf(w, o[u][q].y, acc[4 * q + 1]);
+            acc[4 * q + 2] = fmaf(w, o[u][q].z, acc[4 * q + 2]);
+            acc[4 * q + 3] = fmaf(w, o[u][q].w, acc[4 * q + 3]);
+          }
+        }
+      }
+      lse = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
     }
-  }
-  const float inv = den > 0.f ? 1.0f / den : 0.f;
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-  uint2 v;
-  v.x = *reinterpret_cast<uint32_t*>(&lo);
-  v.y = *reinterpret_cast<uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(chunk + ((int64_t)row * Hg + hl) * kDv + dim) = v;
-  if (threadIdx.x == 0) {
-    const float lse = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
-    const uint32_t bits = __float_as_uint(lse);
-    uint16_t* lp = chunk + (int64_t)R * Hg * kDv + ((int64_t)row * Hg + hl) * 2;
-    lp[0] = (uint16_t)(bits & 0xFFFFu);
-    lp[1] = (uint16_t)(bits >> 16);
+    const float inv = kOne ? (den > 0.f ? 1.f : 0.f) : (den > 0.f ? 1.0f / den : 0.f);
+    float lo[8], hi[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) lo[c] = acc[c], hi[c] = acc[8 + c];
+    uint4* dst = reinterpret_cast<uint4*>(chunk + ((int64_t)row * Hg + hl) * kDv + 16 * lane);
+    dst[0] = f32_to_bf16x8(lo, inv);
+    dst[1] = f32_to_bf16x8(hi, inv);
+    if (lane == 0) {
+      uint32_t* lp = reinterpret_cast<uint32_t*>(chunk + (int64_t)R * Hg * kDv +
+                                                 ((int64_t)row * Hg + hl) * 2);
+      *lp = __float_as_uint(lse);  // the low 16 bits first, then the high (little-endian)
+    }
   }
 }
 
-__global__ void __launch_bounds__(128)
-a2a_combine_kernel(int R, int H, int G, int P, const uint16_t* __restrict__ recv,
+// kW BF16 values (kW = 4: 8 bytes, kW = 8: 16 bytes) as one load or store
+template <int kW> struct BfVec;
+template <> struct BfVec<4> {
+  using T = uint2;
+  static __device__ __forceinline__ void words(const T& v, uint32_t (&w)[2]) { w[0] = v.x, w[1] = v.y; }
+  static __device__ __forceinline__ T make(const uint32_t (&w)[2]) { return make_uint2(w[0], w[1]); }
+};
+template <> struct BfVec<8> {
+  using T = uint4;
+  static __device__ __forceinline__ void words(const T& v, uint32_t (&w)[4]) {
+    w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+  }
+  static __device__ __forceinline__ T make(const uint32_t (&w)[4]) {
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// Lanes given to one combine entry of nch chunks: the power of two at or above nch, at
+// most 32.
+__host__ __device__ inline int lanes_per_entry(int nch) {
+  int l = 1;
+  while (l < nch && l < 32) l <<= 1;
+  return l;
+}
+
+// One warp per (destination, row, head of its slice), grid-stride: lane l owns the
+// kW-value chunks l, l + 32, ... of the P values (narrow payloads: lpe lanes per
+// entry, several entries per warp). One pass over the sources with a
+// running maximum of their LSEs (natural log), four sources' loads in flight together.
+template <int kW>
+__global__ void __launch_bounds__(32 * kXWarps)
+a2a_combine_kernel(int R, int H, int G, int P, int num_dst, const uint16_t* __restrict__ recv,
                    int64_t src_stride, int64_t dst_stride, int dst_begin,
                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+  using V = BfVec<kW>;
+  using T = typename V::T;
+  constexpr int kC = kDv / kW / 32;  // chunks per lane at the largest payload
+  constexpr int kSrc = 4;            // sources whose loads are in flight together
   const int Hg = H / G;
-  const int e = blockIdx.x;  // row * Hg + hl
-  const int di = blockIdx.y;
-  const int row = e / Hg, hl = e % Hg;
-  const int h = (dst_begin + di) * Hg + hl;
-  const uint16_t* base = recv + (int64_t)di * dst_stride;
-  const int64_t lse_off = (int64_t)R * Hg * P + (int64_t)e * 2;
-  auto lse_of = [&](int s) {
-    const uint16_t* lp = base + (int64_t)s * src_stride + lse_off;
-    return __uint_as_float((uint32_t)lp[0] | ((uint32_t)lp[1] << 16));
-  };
-  // one pass with a running maximum over the sources' LSEs (natural log)
-  float M = -INFINITY;
-  float den = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int dim = threadIdx.x * 4;
-  const bool active = dim < P;
-  constexpr int kBatch = 4;  // sources whose loads are in flight together
-  for (int s0 = 0; s0 < G; s0 += kBatch) {
-    float ls[kBatch];
-    uint2 v[kBatch];
+  const int nch = P / kW;
+  // a warp combines 32 / lpe entries side by side (no lane talks to another)
+  const int lpe = lanes_per_entry(nch);
+  const int epw = 32 / lpe;
+  const int lane = (threadIdx.x & 31) & (lpe - 1);
+  const int64_t per_dst = (int64_t)R * Hg;
+  const int64_t n_entries = (int64_t)num_dst * per_dst;
+  const int64_t stride = (int64_t)gridDim.x * kXWarps * epw;
+  for (int64_t g = ((int64_t)blockIdx.x * kXWarps + (threadIdx.x >> 5)) * epw +
+                   (threadIdx.x & 31) / lpe;
+       g < n_entries; g += stride) {
+    const int di = (int)(g / per_dst);
+    const int e = (int)(g - (int64_t)di * per_dst);  // row * Hg + hl
+    const int row = e / Hg, hl = e - row * Hg;
+    const int h = (dst_begin + di) * Hg + hl;
+    const uint16_t* base = recv + (int64_t)di * dst_stride;
+    const int64_t lse_off = (int64_t)R * Hg * P + (int64_t)e * 2;
+    float M = -INFINITY, den = 0.f;
+    float acc[kC][kW];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int s = min(s0 + u, G - 1);
-      ls[u] = s0 + u < G ? lse_of(s) : -INFINITY;
-      v[u] = active ? *reinterpret_cast<const uint2*>(base + (int64_t)s * src_stride +
-                                                       (int64_t)e * P + dim)
-                    : make_uint2(0u, 0u);
-    }
-    float Mb = M;
+    for (int c = 0; c < kC; ++c)
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) Mb = fmaxf(Mb, ls[u]);
-    if (Mb == -INFINITY) continue;
-    if (Mb != M) {
-      const float a = M == -INFINITY ? 0.f : expf(M - Mb);
-      den *= a;
-      acc.x *= a;
-      acc.y *= a;
-      acc.z *= a;
-      acc.w *= a;
-      M = Mb;
-    }
+      for (int q = 0; q < kW; ++q) acc[c][q] = 0.f;
+    for (int s0 = 0; s0 < G; s0 += kSrc) {
+      float ls[kSrc];
+      T v[kSrc][kC];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      if (ls[u] == -INFINITY) continue;
-      const float w = expf(ls[u] - M);
-      den += w;
-      const float2 a2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[u].x));
-      const float2 b2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[u].y));
-      acc.x = fmaf(w, a2.x, acc.x);
-      acc.y = fmaf(w, a2.y, acc.y);
-      acc.z = fmaf(w, b2.x, acc.z);
-      acc.w = fmaf(w, b2.y, acc.w);
+      for (int u = 0; u < kSrc; ++u) {
+        const int s = s0 + u;
+        ls[u] = -INFINITY;
+        if (s < G) {
+          const uint16_t* src = base + (int64_t)s * src_stride;
+          ls[u] = __uint_as_float(*reinterpret_cast<const uint32_t*>(src + lse_off));
+          const T* ent = reinterpret_cast<const T*>(src + (int64_t)e * P);
+#pragma unroll
+          for (int c = 0; c < kC; ++c)
+            if (lane + lpe * c < nch) v[u][c] = ent[lane + lpe * c];
+        }
+      }
+      float Mb = M;
+#pragma unroll
+      for (int u = 0; u < kSrc; ++u) Mb = fmaxf(Mb, ls[u]);
+      if (Mb == -INFINITY) continue;
+      if (Mb != M) {
+        const float a = M == -INFINITY ? 0.f : expf(M - Mb);
+        den *= a;
+#pragma unroll
+        for (int c = 0; c < kC; ++c)
+#pragma unroll
+          for (int q = 0; q < kW; ++q) acc[c][q] *= a;
+        M = Mb;
+      }
+#pragma unroll
+      for (int u = 0; u < kSrc; ++u) {
+        if (ls[u] == -INFINITY) continue;
+        const float w = expf(ls[u] - M);
+        den += w;
+#pragma unroll
+        for (int c = 0; c < kC; ++c) {
+          if (lane + lpe * c >= nch) continue;
+          uint32_t wd[kW / 2];
+          V::words(v[u][c], wd);
+#pragma unroll
+          for (int q = 0; q < kW / 2; ++q) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[q]));
+            acc[c][2 * q] = fmaf(w, f.x, acc[c][2 * q]);
+            acc[c][2 * q + 1] = fmaf(w, f.y, acc[c][2 * q + 1]);
+          }
+        }
+      }
     }
+    const float inv = den > 0.f ? 1.0f / den : 0.f;
+    T* dst = reinterpret_cast<T*>(out + ((int64_t)row * H + h) * P);
+#pragma unroll
+    for (int c = 0; c < kC; ++c) {
+      if (lane + lpe * c >= nch) continue;
+      uint32_t wd[kW / 2];
+#pragma unroll
+      for (int q = 0; q < kW / 2; ++q) {
+        __nv_bfloat162 t = __floats2bfloat162_rn(acc[c][2 * q] * inv, acc[c][2 * q + 1] * inv);
+        wd[q] = *reinterpret_cast<uint32_t*>(&t);
+      }
+      dst[lane + lpe * c] = V::make(wd);
+    }
+    if (lane == 0) lse[(int64_t)row * H + h] = den > 0.f ? M + logf(den) : -INFINITY;
   }
-  const float inv = den > 0.f ? 1.0f / den : 0.f;
-  if (active) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    uint2 v;
-    v.x = *reinterpret_cast<uint32_t*>(&lo);
-    v.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(out + ((int64_t)row * H + h) * P + dim) = v;
-  }
-  if (threadIdx.x == 0) lse[(int64_t)row * H + h] = den > 0.f ? M + logf(den) : -INFINITY;
+}
+
+// Grid of a warp-per-entry kernel: every entry covered, at most a few waves of the
+// SMs' resident CTAs (the loop strides over the rest).
+static unsigned entry_grid(int64_t n_entries) {
+  const int64_t want = (n_entries + kXWarps - 1) / kXWarps;
+  return (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, 152 * 8));
 }
 
 constexpr int kProjVecs = 128;                  // vectors per CTA (MMA M)
@@ -413,11 +502,11 @@ cudaError_t launch_a2a_pack(const dcp_mla_dims& d, const Derived& x, int num_ran
                             void* send, cudaStream_t stream) {
   const int G = d.dcp;
   const int64_t cw = a2a_chunk_words(x.rows, d.num_heads / G, kDv);
-  dim3 grid((unsigned)(x.rows * d.num_heads), (unsigned)num_ranks);
-  // a single split needs no batch (fewer registers, more resident CTAs)
-  auto kern = d.num_splits == 1 ? a2a_pack_kernel<1> : a2a_pack_kernel<4>;
-  kern<<<grid, 128, 0, stream>>>(x.rows, d.num_heads, G, d.num_splits, cw, part_o, part_m, part_l,
-                                 reinterpret_cast<uint16_t*>(send));
+  const int64_t n = (int64_t)num_ranks * x.rows * d.num_heads;
+  auto kern = d.num_splits == 1 ? a2a_pack_kernel<true> : a2a_pack_kernel<false>;
+  kern<<<entry_grid(n), 32 * kXWarps, 0, stream>>>(
+      x.rows, d.num_heads, G, d.num_splits, num_ranks, cw, part_o, part_m, part_l,
+      reinterpret_cast<uint16_t*>(send));
   return cudaGetLastError();
 }
 
@@ -453,10 +542,15 @@ cudaError_t launch_a2a_combine(const dcp_mla_dims& d, const Derived& x, int payl
                                int dst_begin, int num_dst, void* out, float* lse,
                                cudaStream_t stream) {
   const int G = d.dcp;
-  dim3 grid((unsigned)(x.rows * (d.num_heads / G)), (unsigned)num_dst);
-  a2a_combine_kernel<<<grid, 128, 0, stream>>>(
-      x.rows, d.num_heads, G, payload, reinterpret_cast<const uint16_t*>(recv), src_stride,
-      dst_stride, dst_begin, reinterpret_cast<__nv_bfloat16*>(out), lse);
+  const int64_t n = (int64_t)num_dst * x.rows * (d.num_heads / G);
+  // 16-byte chunks when every entry and the output rows start on a 16-byte boundary
+  const bool wide = payload % 8 == 0 && ((uintptr_t)out & 15) == 0;
+  const int nch = payload / (wide ? 8 : 4);
+  const int lpe = lanes_per_entry(nch);
+  auto kern = wide ? a2a_combine_kernel<8> : a2a_combine_kernel<4>;
+  kern<<<entry_grid((n + 32 / lpe - 1) / (32 / lpe)), 32 * kXWarps, 0, stream>>>(
+      x.rows, d.num_heads, G, payload, num_dst, reinterpret_cast<const uint16_t*>(recv),
+      src_stride, dst_stride, dst_begin, reinterpret_cast<__nv_bfloat16*>(out), lse);
   return cudaGetLastError();
 }
 

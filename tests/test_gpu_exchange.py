@@ -252,3 +252,39 @@ def test_partial_packed_rejects_more_than_one_split(dm):
     with pytest.raises(dm.DcpError) as ei:
         ex.partial_packed(w.q, w.kv, scale, w.softmax_scale)
     assert ei.value.code == dm.DCP_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("P,offset", [(12, 0), (40, 0), (40, 4), (512, 0), (512, 4)])
+def test_combine_matches_oracle_combine_on_wire_buffers(dm, P, offset):
+    """dcp_a2a_combine on wire buffers written by the oracle's pack: each destination's
+    merge of the BF16 values it received, within one BF16 ulp of the oracle's fp64
+    combine of the same bits (LSE within float rounding). Payloads that are not a
+    multiple of 8, and outputs that start 8 bytes past a 16-byte boundary (offset 4),
+    take the kernel's 8-byte chunks; the rest its 16-byte chunks."""
+    Bt, S, H, G = 3, 2, 16, 4
+    R = Bt * S
+    dims = dm.make_dims(batch=Bt, qlen=S, num_heads=H, dcp=G, interleave=1, block_size=64,
+                        max_blocks_per_seq=4, max_local_len=256, num_blocks=16, num_splits=1)
+    rng = np.random.default_rng(P + offset)
+    rank_out = rng.standard_normal((G, R, H, P))
+    rank_lse = rng.normal(0.0, 3.0, (G, R, H))
+    rank_lse[rng.random((G, R, H)) < 0.2] = -np.inf       # empty ranks
+    rank_lse[:, 0, 0] = -np.inf                            # an entry no rank reaches
+    rank_out[np.isneginf(rank_lse)] = 0.0
+    recv = X.exchange(X.pack(rank_out, rank_lse))          # [d][s][cw]
+    out_ref, lse_ref = X.combine(recv, R, H, P)
+    cw = X.chunk_words(R, H // G, P)
+    assert cw == dm.dcp_a2a_chunk_words(dims, P)
+    dev_recv = torch.from_numpy(recv.reshape(-1).view(np.int16)).cuda().view(torch.bfloat16)
+    buf = torch.full((offset + R * H * P,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = buf[offset:]
+    lse = torch.full((R, H), float("nan"), dtype=torch.float32, device="cuda")
+    dm.dcp_a2a_combine(dims, P, dev_recv, cw, G * cw, 0, G, out, lse)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy().astype(np.float64).reshape(R, H, P)
+    assert not np.isnan(got).any()
+    assert np.all(np.abs(got - out_ref) <= oracle.fp8.bf16_ulp(out_ref)), P
+    gl = lse.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isneginf(gl), np.isneginf(lse_ref))
+    fin = np.isfinite(lse_ref)
+    assert np.abs(gl[fin] - lse_ref[fin]).max() <= 1e-5 * (1 + np.abs(lse_ref[fin]).max())
