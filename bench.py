@@ -309,12 +309,15 @@ def setup(config, dev, splits=0, batch=0):
 
     # batch: fewer sequences of the same shape (a small case for profiler captures)
     w = workloads.generate(config, device=dev, overrides=dict(batch=batch) if batch else None)
-    ns = splits or dm.choose_num_splits(w.batch, w.qlen, w.num_heads, w.dcp,
-                                        w.max_local_len, w.block_size, dm.num_sms(dev))
+    if splits:
+        ns, base = splits, 0
+    else:  # the static split count, with room for wave balancing where it helps
+        ns, base = dm.choose_split_plan(w.batch, w.qlen, w.num_heads, w.dcp, w.max_local_len,
+                                        w.block_size, dm.concurrent_items())
     dims = dm.make_dims(batch=w.batch, qlen=w.qlen, num_heads=w.num_heads, dcp=w.dcp,
                         interleave=w.interleave, block_size=w.block_size,
                         max_blocks_per_seq=w.max_blocks_per_seq, max_local_len=w.max_local_len,
-                        num_blocks=w.num_blocks, num_splits=ns)
+                        num_blocks=w.num_blocks, num_splits=ns, base_splits=base)
     kvt = dm.KV_FP8_E4M3 if w.kv_dtype == "fp8" else dm.KV_BF16
     step = dm.VerifyStep(dims, kvt, dev)
     scale = torch.tensor([w.kv_scale], dtype=torch.float32, device=dev)
@@ -322,7 +325,7 @@ def setup(config, dev, splits=0, batch=0):
     flush = None
     if kv_bytes < 4 * 129 * 2**20:
         flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=dev)
-    return dict(w=w, ns=ns, dims=dims, kvt=kvt, step=step, scale=scale, flush=flush,
+    return dict(w=w, ns=ns, base=base, dims=dims, kvt=kvt, step=step, scale=scale, flush=flush,
                 kv_bytes=kv_bytes)
 
 
@@ -371,6 +374,13 @@ def time_packed(env, K, warmup, stream):
     import decode_context_mla_causal_gb300 as dm
 
     w, step, scale = env["w"], env["step"], env["scale"]
+    if env["ns"] != 1:  # the fused epilogue takes one split: a one-split step of the same dims
+        d = env["dims"]
+        step = dm.VerifyStep(dm.make_dims(
+            batch=d.batch, qlen=d.qlen, num_heads=d.num_heads, dcp=d.dcp, interleave=d.interleave,
+            block_size=d.block_size, max_blocks_per_seq=d.max_blocks_per_seq,
+            max_local_len=d.max_local_len, num_blocks=d.num_blocks, num_splits=1,
+            causal=bool(d.causal)), env["kvt"], w.q.device)
     ex = dm.A2AExchange(step)
     step.metadata(w.seq_lens, w.block_table)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
@@ -437,7 +447,15 @@ def time_a2a(env, K, warmup, stream):
         avg = [1e3 * sum(e[j].elapsed_time(e[j + 1]) for e in a_ev) / K for j in range(3)]
         packed_bytes = ex.packed.numel() * 2
         send_bytes = ex.send.numel() * 2
-        pack_bytes = nr * ns * R * H * (4 * 512 + 8) + packed_bytes
+        # partials whose output the pack reads: every slot, or with wave balancing
+        # the live ones (slot 0 and the non-empty slots; their m and l are read for all)
+        slots = nr * w.batch * ns
+        if env["base"]:
+            beg, end = step.split_beg.cpu(), step.split_end.cpu()
+            live = (end > beg)
+            live[:, :, 0] = True
+            slots = int(live.sum())
+        pack_bytes = (slots * w.qlen * H * 4 * 512 + nr * ns * R * H * 8) + packed_bytes
         comb_bytes = send_bytes + R * H * (2 * ex.payload + 4)
         a2a[label] = {"payload": ex.payload, "send_bytes": send_bytes,
                       "kernel_us": {"pack": avg[0], "combine": avg[2]},
@@ -604,6 +622,7 @@ def main():
                    "global_batch": w.batch * world, "seq_len": int(w.seq_lens.max()),
                    "qlen": w.qlen, "num_heads": w.num_heads, "dcp": w.dcp,
                    "interleave": w.interleave, "num_splits": ns,
+                   "base_splits": env["base"],
                    "parallelism": f"dcp{w.dcp} virtual shards per GPU; replicas x{world}",
                    "l2": ("flushed with a 512 MB write before each timed step" if flush is not None
                           else f"inputs larger than L2 (cache {env['kv_bytes'] / 1e9:.2f} GB)")},
@@ -653,7 +672,7 @@ def main():
                 cpart = sum(ct["part"]) / K
                 ach, tp, hp, croof = roofline(cfl, cby, cpart, peaks)
                 entry = {"workload": f"{cfg} {workloads.DESCRIPTIONS[cfg]}",
-                         "num_splits": e["ns"], "ms_per_step": cms,
+                         "num_splits": e["ns"], "base_splits": e["base"], "ms_per_step": cms,
                          "value": ctok * K / (sum(ct["step"]) / 1e3), "unit": UNIT,
                          "tflops": cfl / (cms / 1e3) / 1e12,
                          "kernel_us": {"metadata": 1e3 * sum(ct["meta"]) / K,
@@ -668,7 +687,7 @@ def main():
                                 if e["flush"] is not None else "inputs larger than L2")}
                 if cfg in ("c3", "c4"):  # the exchange at the sizes where HBM rate means something
                     entry["a2a"] = time_a2a(e, K, args.warmup, stream)
-                if e["ns"] == 1 and cw.num_heads % cw.dcp == 0:
+                if cfg in ("c3", "c4") and cw.num_heads % cw.dcp == 0:
                     entry["a2a_one_split"] = time_packed(e, K, args.warmup, stream)
                 if not args.no_cpu_baseline:
                     entry["cpu_baseline"], entry["parity"] = cpu_baseline(

@@ -46,7 +46,8 @@ class Dims(ctypes.Structure):
 
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "qlen", "num_heads", "dcp", "interleave", "block_size",
-        "max_blocks_per_seq", "max_local_len", "num_blocks", "num_splits", "causal")]
+        "max_blocks_per_seq", "max_local_len", "num_blocks", "num_splits", "causal",
+        "base_splits")]
 
     def __repr__(self):
         return "Dims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
@@ -80,6 +81,7 @@ def load() -> ctypes.CDLL:
     sig = {
         "dcp_mla_subpage_size": (I, [I]),
         "dcp_mla_max_pages": (I, [D]),
+        "dcp_mla_concurrent_items": (I, []),
         "dcp_mla_check_dims": (I, [D, I, I]),
         "dcp_mla_metadata": (I, [D, P, P, I, I, P, P, P, P, P, P]),
         "dcp_mla_partial": (I, [D, P, P, I, P, ctypes.c_float, I, I, P, P, P, P, P, P, P, P, P,
@@ -146,6 +148,11 @@ def dcp_mla_subpage_size(block_size: int) -> int:
 
 def dcp_mla_max_pages(dims: Dims) -> int:
     return load().dcp_mla_max_pages(ctypes.byref(dims))
+
+
+def dcp_mla_concurrent_items() -> int:
+    """Work items the partial kernel runs at once on the current device (-1: none)."""
+    return int(load().dcp_mla_concurrent_items())
 
 
 def dcp_mla_check_dims(dims: Dims, rank_begin: int = 0, num_ranks: int | None = None):

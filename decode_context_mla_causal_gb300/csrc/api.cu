@@ -64,6 +64,13 @@ static dcp_status check(const dcp_mla_dims* d, int32_t rank_begin, int32_t num_r
     return fail(DCP_ERR_INVALID_ARG, "num_splits must be in [1, 4096] (got %d)", d->num_splits);
   if (d->causal != 0 && d->causal != 1)
     return fail(DCP_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (d->base_splits < 0 || d->base_splits > d->num_splits)
+    return fail(DCP_ERR_INVALID_ARG, "base_splits must be in [0, num_splits=%d] (got %d)",
+                d->num_splits, d->base_splits);
+  if (d->base_splits > 0 && d->base_splits < d->num_splits &&
+      (int64_t)d->batch * d->dcp > kBalanceMaxPairs)
+    return fail(DCP_ERR_UNSUPPORTED, "wave balancing takes at most %d (rank, sequence) pairs",
+                kBalanceMaxPairs);
   if ((int64_t)d->batch * d->qlen * d->num_heads > (int64_t)(1 << 24))
     return fail(DCP_ERR_UNSUPPORTED, "batch*qlen*num_heads above 2^24");
   if (rank_begin < 0 || num_ranks < 1 || (int64_t)rank_begin + num_ranks > d->dcp)
@@ -295,6 +302,8 @@ dcp_status dcp_a2a_combine(const dcp_mla_dims* dims, int32_t payload, const void
                                      num_dst, out, lse, (cudaStream_t)stream),
                   "dcp_a2a_combine");
 }
+
+int32_t dcp_mla_concurrent_items(void) { return partial_concurrent_items(); }
 
 const char* dcp_last_error(void) { return g_last_error.c_str(); }
 

@@ -41,6 +41,18 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
 // Device workspace launch_partial uses for the item order (bytes, 16-byte multiple).
 size_t partial_workspace_bytes(const dcp_mla_dims& d, int num_ranks);
 
+// Clusters of the partial kernel the current device runs at once (cached per
+// device), or a negative value when the query fails.
+int partial_concurrent_items();
+
+// Wave balancing reads every (rank, sequence) pair's length in each metadata CTA.
+constexpr int kBalanceMaxPairs = 1 << 16;
+
+// Tiles of 64 tokens per work item, the unit of the split plan.
+constexpr int kPlanTileTokens = 64;
+// Wave balancing cuts no piece below this many tiles.
+constexpr int kPlanMinPieceTiles = 8;
+
 cudaError_t launch_merge(const dcp_mla_dims& d, const Derived& x, int num_ranks,
                          const float* part_o, const float* part_m, const float* part_l,
                          void* out, float* lse, float* rank_lse, uint32_t* status,

@@ -63,12 +63,16 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8], float scale)
 }
 
 // One warp per (rank, row, head) entry, grid-stride: lane l owns dims [16l, 16l + 16).
-// More than one split: one pass with a running maximum over the splits' m, four
-// splits' loads in flight together, the sums rescaled by 2^(M_old - M_new) when M
-// rises. One split: its normalised output as it is and LSE = (m + log2 l) ln 2 (the
-// same arithmetic as the partial kernel's packed epilogue, so both give the same bits).
-template <bool kOne>  // one split: no merge, fewer registers, more warps resident
-__global__ void __launch_bounds__(32 * kXWarps, kOne ? 4 : 2)
+// More than one split: one pass with a running maximum, the sums rescaled by
+// 2^(M_old - M_new) when M rises; kPackAll reads four splits' m, l and outputs
+// together (every slot expected to hold work), kPackLive reads the m and l of 32
+// splits first and then only the live splits' outputs (wave balancing leaves most
+// slots empty; a skipped slot's m is -inf). One split (kPackOne): its normalised
+// output as it is and LSE = (m + log2 l) ln 2 (the same arithmetic as the partial
+// kernel's packed epilogue, so both give the same bits).
+enum { kPackOne = 0, kPackAll = 1, kPackLive = 2 };
+template <int kMode>
+__global__ void __launch_bounds__(32 * kXWarps, kMode == kPackOne ? 4 : 2)
 a2a_pack_kernel(int R, int H, int G, int num_splits, int num_ranks, int64_t cw,
                 const float* __restrict__ part_o, const float* __restrict__ part_m,
                 const float* __restrict__ part_l, uint16_t* __restrict__ send) {
@@ -95,7 +99,7 @@ a2a_pack_kernel(int R, int H, int G, int num_splits, int num_ranks, int64_t cw,
 #pragma unroll
     for (int c = 0; c < 16; ++c) acc[c] = 0.f;
     float lse;
-    if (kOne) {
+    if (kMode == kPackOne) {
       // the output's loads do not wait for m and l: a dead entry's values are dropped
       const float4* src = reinterpret_cast<const float4*>(part_o + p0 * kDv + 16 * lane);
       float4 v[4];
@@ -113,56 +117,113 @@ a2a_pack_kernel(int R, int H, int G, int num_splits, int num_ranks, int64_t cw,
       den = live ? 1.f : 0.f;
       lse = live ? (m + log2f(l)) * kLn2 : -INFINITY;
     } else {
-      for (int s0 = 0; s0 < num_splits; s0 += 4) {
-        float m[4], l[4];
-        float4 o[4][4];
+      if (kMode == kPackAll) {
+        for (int s0 = 0; s0 < num_splits; s0 += 4) {
+          float m[4], l[4];
+          float4 o[4][4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          m[u] = -INFINITY;
-          l[u] = 0.f;
-          if (s0 + u < num_splits) {  // no load at all past the last split
-            const int64_t i = p0 + (int64_t)(s0 + u) * rows_heads;
-            m[u] = part_m[i];
-            l[u] = part_l[i];
-            const float4* src = reinterpret_cast<const float4*>(part_o + i * kDv + 16 * lane);
+          for (int u = 0; u < 4; ++u) {
+            m[u] = -INFINITY;
+            l[u] = 0.f;
+            if (s0 + u < num_splits) {  // no load at all past the last split
+              const int64_t i = p0 + (int64_t)(s0 + u) * rows_heads;
+              m[u] = part_m[i];
+              l[u] = part_l[i];
+              const float4* src = reinterpret_cast<const float4*>(part_o + i * kDv + 16 * lane);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) o[u][q] = src[q];
-          } else {
+              for (int q = 0; q < 4; ++q) o[u][q] = src[q];
+            } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) o[u][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int q = 0; q < 4; ++q) o[u][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+          float Mb = M;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (!(m[u] != -INFINITY && l[u] > 0.f)) m[u] = -INFINITY;
+            Mb = fmaxf(Mb, m[u]);
+          }
+          if (Mb == -INFINITY) continue;
+          if (Mb != M) {
+            const float a = M == -INFINITY ? 0.f : exp2f(M - Mb);
+            den *= a;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) acc[c] *= a;
+            M = Mb;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (m[u] == -INFINITY) continue;
+            const float w = exp2f(m[u] - M) * l[u];
+            den += w;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[4 * q] = fmaf(w, o[u][q].x, acc[4 * q]);
+              acc[4 * q + 1] = fmaf(w, o[u][q].y, acc[4 * q + 1]);
+              acc[4 * q + 2] = fmaf(w, o[u][q].z, acc[4 * q + 2]);
+              acc[4 * q + 3] = fmaf(w, o[u][q].w, acc[4 * q + 3]);
+            }
           }
         }
-        float Mb = M;
+      } else {
+        // m and l of 32 splits in one load per lane; only live splits' outputs are read,
+        // four at a time (an empty split, or a slot the partial kernel skipped, is -inf)
+        for (int c0 = 0; c0 < num_splits; c0 += 32) {
+          float mi = -INFINITY, li = 0.f;
+          if (c0 + lane < num_splits) {
+            mi = part_m[p0 + (int64_t)(c0 + lane) * rows_heads];
+            li = part_l[p0 + (int64_t)(c0 + lane) * rows_heads];
+          }
+          const bool live = mi != -INFINITY && li > 0.f;
+          if (!live) mi = -INFINITY;
+          unsigned mask = __ballot_sync(0xffffffffu, live);
+          if (mask == 0u) continue;
+          float cm = mi;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (!(m[u] != -INFINITY && l[u] > 0.f)) m[u] = -INFINITY;
-          Mb = fmaxf(Mb, m[u]);
-        }
-        if (Mb == -INFINITY) continue;
-        if (Mb != M) {
-          const float a = M == -INFINITY ? 0.f : exp2f(M - Mb);
-          den *= a;
+          for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+          if (cm > M) {
+            const float a = M == -INFINITY ? 0.f : exp2f(M - cm);
+            den *= a;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) acc[c] *= a;
-          M = Mb;
-        }
+            for (int c = 0; c < 16; ++c) acc[c] *= a;
+            M = cm;
+          }
+          const float wi = live ? exp2f(mi - M) * li : 0.f;
+          while (mask != 0u) {  // warp-uniform
+            int src[4];
+            float w[4];
+            float4 o[4][4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (m[u] == -INFINITY) continue;
-          const float w = exp2f(m[u] - M) * l[u];
-          den += w;
+            for (int u = 0; u < 4; ++u) {
+              src[u] = mask != 0u ? __ffs(mask) - 1 : -1;
+              if (mask != 0u) mask &= mask - 1u;
+              w[u] = __shfl_sync(0xffffffffu, wi, src[u] < 0 ? 0 : src[u]);
+              if (src[u] >= 0) {
+                const float4* po = reinterpret_cast<const float4*>(
+                    part_o + (p0 + (int64_t)(c0 + src[u]) * rows_heads) * kDv + 16 * lane);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            acc[4 * q] = fmaf(w, o[u][q].x, acc[4 * q]);
-            acc[4 * q + 1] = fmaf(w, o[u][q].y, acc[4 * q + 1]);
-            acc[4 * q + 2] = fmaf(w, o[u][q].z, acc[4 * q + 2]);
-            acc[4 * q + 3] = fmaf(w, o[u][q].w, acc[4 * q + 3]);
+                for (int q = 0; q < 4; ++q) o[u][q] = po[q];
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (src[u] < 0) continue;
+              den += w[u];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                acc[4 * q] = fmaf(w[u], o[u][q].x, acc[4 * q]);
+                acc[4 * q + 1] = fmaf(w[u], o[u][q].y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(w[u], o[u][q].z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(w[u], o[u][q].w, acc[4 * q + 3]);
+              }
+            }
           }
         }
       }
       lse = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
     }
-    const float inv = kOne ? (den > 0.f ? 1.f : 0.f) : (den > 0.f ? 1.0f / den : 0.f);
+    const float inv =
+        kMode == kPackOne ? (den > 0.f ? 1.f : 0.f) : (den > 0.f ? 1.0f / den : 0.f);
     float lo[8], hi[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) lo[c] = acc[c], hi[c] = acc[8 + c];
@@ -503,7 +564,9 @@ cudaError_t launch_a2a_pack(const dcp_mla_dims& d, const Derived& x, int num_ran
   const int G = d.dcp;
   const int64_t cw = a2a_chunk_words(x.rows, d.num_heads / G, kDv);
   const int64_t n = (int64_t)num_ranks * x.rows * d.num_heads;
-  auto kern = d.num_splits == 1 ? a2a_pack_kernel<true> : a2a_pack_kernel<false>;
+  auto kern = d.num_splits == 1                                     ? a2a_pack_kernel<kPackOne>
+              : d.base_splits > 0 && d.base_splits < d.num_splits ? a2a_pack_kernel<kPackLive>
+                                                                   : a2a_pack_kernel<kPackAll>;
   kern<<<entry_grid(n), 32 * kXWarps, 0, stream>>>(
       x.rows, d.num_heads, G, d.num_splits, num_ranks, cw, part_o, part_m, part_l,
       reinterpret_cast<uint16_t*>(send));

@@ -157,6 +157,7 @@ struct Params {
   float* part_l;
   uint32_t* status;
   const int32_t* item_order;  // cluster -> work item (longest first), or null: natural order
+  const int32_t* n_live;      // clusters with an item in item_order (the rest exit at once)
   // packed epilogue (one split): the all-to-all send buffers [rank][G][cw words] get the
   // BF16 output and the LSE words instead of part_o/m/l (null: the fp32 partials)
   uint16_t* send;
@@ -991,6 +992,19 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
   if (row_ok && cta == 0 && h == 0) {
     p.part_m[base] = l_run > 0.f ? M : -INFINITY;
     p.part_l[base] = l_run;
+    if (it.s == 0) {
+      // the empty slots s >= 1 of this (rank, sequence) run no item of their own when
+      // the order kernel drops them: their m and l are written here (their output
+      // is never read)
+      const int64_t sb0 = ((int64_t)it.k * p.batch + it.b) * p.num_splits;
+      const int64_t slot = (int64_t)R * p.H;
+      for (int s2 = 1; s2 < p.num_splits; ++s2) {
+        if (p.split_end[sb0 + s2] <= p.split_beg[sb0 + s2]) {
+          p.part_m[base + s2 * slot] = -INFINITY;
+          p.part_l[base + s2 * slot] = 0.f;
+        }
+      }
+    }
   }
 }
 
@@ -1000,10 +1014,11 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
 // order_kernel sorts the items by tile count, longest first, which brings list
 // scheduling within a few percent of the ideal makespan. The sort is over groups
 // (rank, sequence, split): a group's row tiles read the same cache rows, so they
-// stay adjacent and run side by side, sharing those rows in L2. One CTA: a
-// histogram over (clamped) group tile counts, an exclusive scan, a scatter. Groups
-// with equal counts land in any order; no item's result depends on the cluster
-// that computes it.
+// stay adjacent and run side by side, sharing those rows in L2. Groups of empty
+// slots s >= 1 (split_beg == split_end) are left out; slot 0's items write their
+// m and l. One CTA: a histogram over (clamped) group tile counts, an exclusive
+// scan, a scatter; then the number of listed items. Groups with equal counts land
+// in any order; no item's result depends on the cluster that computes it.
 constexpr int kOrderThreads = 1024;
 constexpr int kOrderBuckets = 4096;  // tile counts at or above the last bucket share it
 constexpr int kOrderMaxItems = 1 << 16;
@@ -1016,12 +1031,17 @@ __global__ void __launch_bounds__(kOrderThreads) order_kernel(const Params p, in
   for (int b = tid; b < kOrderBuckets; b += kOrderThreads) bucket[b] = 0;
   __syncthreads();
   const int rt = p.n_row_tiles;
+  // group g = (rank, sequence, split) in natural order is also its split-bound index
+  auto dropped = [&](int g) {
+    return g % p.num_splits != 0 && p.split_end[g] <= p.split_beg[g];
+  };
   auto key_of = [&](int g) {
     int tiles = 0;
     for (int t = 0; t < rt; ++t) tiles = max(tiles, decode_item(p, g * rt + t).n_tiles);
     return kOrderBuckets - 1 - min(tiles, kOrderBuckets - 1);
   };
-  for (int g = tid; g < n_groups; g += kOrderThreads) atomicAdd(&bucket[key_of(g)], 1);
+  for (int g = tid; g < n_groups; g += kOrderThreads)
+    if (!dropped(g)) atomicAdd(&bucket[key_of(g)], 1);
   __syncthreads();
   // exclusive scan of the buckets, 4 per thread
   constexpr int kPer = kOrderBuckets / kOrderThreads;
@@ -1058,9 +1078,12 @@ __global__ void __launch_bounds__(kOrderThreads) order_kernel(const Params p, in
   }
   __syncthreads();
   for (int g = tid; g < n_groups; g += kOrderThreads) {
+    if (dropped(g)) continue;
     const int pos = atomicAdd(&bucket[key_of(g)], 1);
     for (int t = 0; t < rt; ++t) order[pos * rt + t] = g * rt + t;
   }
+  // listed groups = the inclusive total over all warps
+  if (tid == 0) order[n_groups * rt] = warp_total[kOrderThreads / 32 - 1] * rt;
 }
 
 template <bool kFp8>
@@ -1074,6 +1097,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
   const int cta = (int)cluster_ctarank();
   const int cluster_id = blockIdx.x >> 1;
+  // clusters past the listed items have nothing to do (both CTAs of a cluster agree,
+  // and neither has touched a barrier or tensor memory yet)
+  if (p.n_live != nullptr && cluster_id >= *p.n_live) return;
   const Item it = decode_item(p, p.item_order ? p.item_order[cluster_id] : cluster_id);
 
   if (tid == 0) {
@@ -1156,6 +1182,7 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
   p.part_l = part_l;
   p.status = status;
   p.item_order = nullptr;
+  p.n_live = nullptr;
   p.send = reinterpret_cast<uint16_t*>(send);
   p.G = d.dcp;
   p.send_cw = send ? a2a_chunk_words(d.batch * d.qlen, d.num_heads / d.dcp, kDv) : 0;
@@ -1188,6 +1215,7 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     p.item_order = order;
+    p.n_live = order + items;
   }
   kern<<<(unsigned)(items * 2), kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
@@ -1196,7 +1224,27 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
 size_t partial_workspace_bytes(const dcp_mla_dims& d, int num_ranks) {
   const int64_t items = (int64_t)((d.qlen * d.num_heads + kRows - 1) / kRows) * d.num_splits *
                         d.batch * num_ranks;
-  return (size_t)((items * 4 + 15) / 16 * 16);
+  return (size_t)(((items + 1) * 4 + 15) / 16 * 16);  // the order, then the listed count
+}
+
+int partial_concurrent_items() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  if (cached[dev] > 0) return cached[dev];
+  // both instantiations take the same threads and shared memory
+  auto kern = partial_tc_kernel<true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+      cudaSuccess)
+    return -1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 4096);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;  // cluster shape from the kernel's own attribute
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return -1;
+  cached[dev] = n;
+  return n;
 }
 
 }  // namespace dcpmla

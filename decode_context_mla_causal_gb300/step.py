@@ -45,10 +45,40 @@ def choose_num_splits(batch: int, qlen: int, num_heads: int, num_ranks: int,
     return int(best[1])
 
 
+def concurrent_items() -> int:
+    """Work items the partial kernel runs at once on the current device."""
+    n = B.dcp_mla_concurrent_items()
+    if n < 1:
+        raise RuntimeError("no CUDA device to size the split plan for")
+    return n
+
+
+def choose_split_plan(batch: int, qlen: int, num_heads: int, num_ranks: int,
+                      max_local_len: int, block_size: int, concurrent: int = 76):
+    """``(num_splits, base_splits)`` for the dims: the static split count of
+    ``choose_num_splits`` as the base and, when the work items at the static bound
+    leave the last wave of ``concurrent`` items at most half full, room for the
+    shortest (rank, sequence) pairs to take more splits and fill it (the device's
+    wave balancing, ``dcp_mla_metadata``). ``base_splits`` is 0 when there is
+    nothing to balance."""
+    base = choose_num_splits(batch, qlen, num_heads, num_ranks, max_local_len, block_size,
+                             sms=2 * concurrent)
+    tiles = max(1, math.ceil(max_local_len / 64))
+    per = math.ceil(qlen * num_heads / 128) * base
+    rem = batch * num_ranks * per % concurrent
+    if rem == 0 or 2 * rem > concurrent:
+        return base, 0
+    tail = -(-rem // per)
+    kf = concurrent // (tail * per)
+    hi = (concurrent - kf * tail * per) // per
+    ns = min(64, base * (max(1, kf) + (1 if hi > 0 else 0)), max(base, tiles // 8))
+    return (ns, base) if ns > base else (base, 0)
+
+
 def make_dims(*, batch, qlen, num_heads, dcp, interleave, block_size, max_blocks_per_seq,
-              max_local_len, num_blocks, num_splits, causal=True) -> B.Dims:
+              max_local_len, num_blocks, num_splits, causal=True, base_splits=0) -> B.Dims:
     return B.Dims(batch, qlen, num_heads, dcp, interleave, block_size, max_blocks_per_seq,
-                  max_local_len, num_blocks, num_splits, 1 if causal else 0)
+                  max_local_len, num_blocks, num_splits, 1 if causal else 0, base_splits)
 
 
 class VerifyStep:

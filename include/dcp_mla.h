@@ -36,8 +36,10 @@
  *     subpage p of a sequence (p < ceil(local_len / P)) is numbered
  *     block_table[b][p / ppb] * ppb + p % ppb (ppb = block_size / P) and covers
  *     rows [page*P, page*P + P) of a rank's flat pool [num_blocks*block_size][576].
- *   - Split s of num_splits covers subpages [s*np/NS, (s+1)*np/NS) (floor) of
- *     the np subpages the longest row of the sequence needs on that rank.
+ *   - A (rank, sequence) cut into n splits: split s < n covers subpages
+ *     [s*np/n, (s+1)*np/n) (floor) of the np subpages the longest row of the
+ *     sequence needs on that rank; slots s >= n are empty ([np, np)). n = NS
+ *     unless wave balancing (dims.base_splits) chooses fewer.
  *
  * Conventions shared by every call:
  *   - Every pointer argument named as device memory must point to device memory
@@ -107,8 +109,14 @@ typedef struct {
                                  be >= max_local_len                           */
   int32_t max_local_len;      /* static bound on every rank-local length       */
   int32_t num_blocks;         /* NB, blocks in each rank's pool                */
-  int32_t num_splits;         /* NS, static split count per (rank, sequence)   */
+  int32_t num_splits;         /* NS, split slots per (rank, sequence)          */
   int32_t causal;             /* 1: per-row causal boundary; 0: whole sequence */
+  int32_t base_splits;        /* 0 (or NS): every (rank, sequence) takes NS
+                                 equal splits. 1..NS-1: wave balancing (see
+                                 dcp_mla_metadata): each takes base_splits,
+                                 and the shortest ones, whose work items would
+                                 otherwise run in a part-filled last wave of the
+                                 device, take more, up to NS                   */
 } dcp_mla_dims;
 
 /* Subpage size for a block size: min(128, largest power of two dividing it),
@@ -142,11 +150,29 @@ dcp_status dcp_mla_check_dims(const dcp_mla_dims* dims, int32_t rank_begin, int3
  *   status      device uint32 [1]          in/out: DCP_STATUS_BAD_SEQ_LEN,
  *                                          _LOCAL_OVER_BOUND, _BAD_BLOCK_ID ORed
  * Every output element is written (bit-exact, padding included).
+ *
+ * Wave balancing (0 < dims.base_splits < NS): the partial kernel runs C work
+ * items at once (C = dcp_mla_concurrent_items()). With every (rank, sequence)
+ * of the whole dcp group cut into base_splits, N = live * row_tiles * base_splits
+ * items (live: pairs with a non-empty longest row; row_tiles =
+ * ceil(qlen*H/128)). If the last wave is at most half full (0 < N mod C <= C/2),
+ * the u = ceil((N mod C) / (row_tiles*base_splits)) shortest live pairs (ties:
+ * the later pair, in rank-major order, is shorter) share the C slots of that wave:
+ * pair j of them takes base_splits*k splits, k = floor(C / (u*row_tiles*
+ * base_splits)) plus one for the first (C - that*u*row_tiles*base_splits) /
+ * (row_tiles*base_splits) of them, at most NS, at most one split per 8 tiles of
+ * 64 tokens, never fewer than base_splits. The choice depends on seq_lens and the
+ * dims only, never on rank_begin/num_ranks, so a per-rank call cuts exactly as
+ * the call for the whole group does.
  */
 dcp_status dcp_mla_metadata(const dcp_mla_dims* dims, const int32_t* seq_lens,
                             const int32_t* block_table, int32_t rank_begin, int32_t num_ranks,
                             int32_t* row_len, int32_t* page_ids, int32_t* split_beg,
                             int32_t* split_end, uint32_t* status, dcp_stream_t stream);
+
+/* Work items (clusters of two CTAs) of dcp_mla_partial that the current device
+ * runs at once; -1 if there is no device or the query fails. Host only. */
+int32_t dcp_mla_concurrent_items(void);
 
 /*
  * Step 3: split-KV absorbed-MLA partial attention on each rank's local KV.
@@ -163,7 +189,9 @@ dcp_status dcp_mla_metadata(const dcp_mla_dims* dims, const int32_t* seq_lens,
  *   row_len, page_ids, split_beg, split_end: dcp_mla_metadata's outputs for the
  *               same dims and ranks
  *   part_o      device float [nr][NS][R][H][512]  out: per-split normalised
- *               output sum_t 2^(s_t - m) v_t / l   (0 for an empty split)
+ *               output sum_t 2^(s_t - m) v_t / l   (0 for an empty split; not
+ *               written for a slot s >= 1 with split_beg == split_end, whose m
+ *               is -inf: readers skip the output of every -inf split)
  *   part_m      device float [nr][NS][R][H]  out: m = max_t s_t, where
  *               s_t = softmax_scale * kv_scale * log2(e) * (q . k_t) (base 2);
  *               -inf for an empty split
@@ -171,9 +199,11 @@ dcp_status dcp_mla_metadata(const dcp_mla_dims* dims, const int32_t* seq_lens,
  *   workspace   device, 16-byte aligned, dcp_mla_workspace_size(dims, num_ranks)
  *               bytes, or NULL. The call first orders the work items (rank,
  *               sequence, split, 128-row tile) by tile count, longest first, so
- *               that items of very different lengths finish together (up to 65536
- *               items; beyond that, and with NULL, items run in their natural
- *               order). The results are bit-identical either way.
+ *               that items of very different lengths finish together, and drops
+ *               the items of empty slots s >= 1 (the item of slot 0 writes their
+ *               m and l). Up to 65536 items; beyond that, and with NULL, every
+ *               item runs, in natural order. part_m, part_l and every part_o that
+ *               readers use are bit-identical either way.
  *   status      device uint32 [1]            in/out: DCP_STATUS_BAD_PAGE,
  *               DCP_STATUS_BAD_SPLIT, DCP_STATUS_TIMEOUT, DCP_STATUS_Q_RANGE
  * Tokens at or beyond a row's length, and pages with invalid ids, never reach

@@ -9,11 +9,18 @@ import oracle
 import workloads
 
 
-def dims_of(dm, w, num_splits, causal=True):
+def dims_of(dm, w, num_splits, causal=True, base_splits=0):
     return dm.make_dims(batch=w.batch, qlen=w.qlen, num_heads=w.num_heads, dcp=w.dcp,
                         interleave=w.interleave, block_size=w.block_size,
                         max_blocks_per_seq=w.max_blocks_per_seq, max_local_len=w.max_local_len,
-                        num_blocks=w.num_blocks, num_splits=num_splits, causal=causal)
+                        num_blocks=w.num_blocks, num_splits=num_splits, causal=causal,
+                        base_splits=base_splits)
+
+
+def split_plan(dm, w):
+    """The product's default (num_splits, base_splits) for a workload on this device."""
+    return dm.choose_split_plan(w.batch, w.qlen, w.num_heads, w.dcp, w.max_local_len,
+                                w.block_size, dm.concurrent_items())
 
 
 def kv_dtype_of(dm, w):
@@ -22,12 +29,12 @@ def kv_dtype_of(dm, w):
 
 def run_gpu(dm, w, num_splits=None, causal=True, rank_begin=0, num_ranks=None, step=None):
     """Run metadata + partial + merge on the workload's device; returns the step."""
+    base = 0
     if num_splits is None:
-        num_splits = dm.choose_num_splits(w.batch, w.qlen, w.num_heads, w.dcp, w.max_local_len,
-                                          w.block_size, dm.num_sms())
+        num_splits, base = split_plan(dm, w)
     if step is None:
-        step = dm.VerifyStep(dims_of(dm, w, num_splits, causal), kv_dtype_of(dm, w), w.q.device,
-                             rank_begin=rank_begin, num_ranks=num_ranks)
+        step = dm.VerifyStep(dims_of(dm, w, num_splits, causal, base), kv_dtype_of(dm, w),
+                             w.q.device, rank_begin=rank_begin, num_ranks=num_ranks)
     nr = step.num_ranks
     kv = w.kv[rank_begin:rank_begin + nr].contiguous()
     scale = torch.tensor([w.kv_scale], dtype=torch.float32, device=w.q.device)
@@ -95,3 +102,67 @@ def assert_parity(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
     st = compare(out_gpu, lse_gpu, out_ref, lse_ref)
     assert st["bad_out"] == 0 and st["bad_lse"] == 0 and st["inf_ok"], (what, st)
     return st
+
+
+def _local_len(g, rank, dcp, interleave):
+    """Local length of a row with global boundary g ("Support Kimi-K3 DCP with
+    DSpark", review thread)."""
+    if g <= 0:
+        return 0
+    span = dcp * interleave
+    rem = min(max(g % span - rank * interleave, 0), interleave)
+    return g // span * interleave + rem
+
+
+def balanced_split_counts(seq_lens, *, batch, qlen, num_heads, dcp, interleave,
+                          max_local_len, num_splits, base_splits, concurrent):
+    """Host restatement of the wave-balancing rule documented beside dcp_mla_metadata:
+    the number of splits each (rank, sequence) pair takes, ``n[rank][b]``."""
+    n = np.full((dcp, batch), num_splits, dtype=np.int64)
+    if not 0 < base_splits < num_splits:
+        return n
+    tiles = np.array([[-(-min(_local_len(max(int(seq_lens[b]), 0), r, dcp, interleave),
+                                 max_local_len) // 64) for b in range(batch)]
+                      for r in range(dcp)])
+    flat = tiles.reshape(-1)                       # rank-major pair index
+    live = int((flat > 0).sum())
+    per = -(-(qlen * num_heads) // 128) * base_splits
+    rem = live * per % concurrent
+    for v in range(flat.size):
+        t = int(flat[v])
+        if t == 0:
+            s = 1
+        elif rem == 0 or 2 * rem > concurrent:
+            s = base_splits
+        else:
+            tail = -(-rem // per)
+            pos = int((flat > t).sum() + (flat[:v] == t).sum())
+            if pos < live - tail:
+                s = base_splits
+            else:
+                j = pos - (live - tail)
+                kf = concurrent // (tail * per)
+                hi = (concurrent - kf * tail * per) // per
+                s = min(base_splits * (max(kf, 1) + (1 if j < hi else 0)), num_splits,
+                        t // 8)
+                s = max(s, base_splits)
+        n.reshape(-1)[v] = s
+    return n
+
+
+def expected_split_bounds(n, row_len, *, batch, qlen, num_splits, subpage, rank_begin=0):
+    """split_beg/split_end for per-pair split counts ``n[rank][b]`` (all ranks) over
+    the call's ranks, from the call's row_len ``[nr][R]``: split s < n of a pair covers
+    subpages [s*np/n, (s+1)*np/n), later slots are [np, np)."""
+    nr = row_len.shape[0]
+    beg = np.zeros((nr, batch, num_splits), dtype=np.int64)
+    end = np.zeros_like(beg)
+    for k in range(nr):
+        for b in range(batch):
+            longest = int(row_len[k, b * qlen:(b + 1) * qlen].max())
+            np_ = -(-longest // subpage)
+            nn = int(n[rank_begin + k, b])
+            for s in range(num_splits):
+                beg[k, b, s] = s * np_ // nn if s < nn else np_
+                end[k, b, s] = (s + 1) * np_ // nn if s < nn else np_
+    return beg, end

@@ -63,6 +63,7 @@ def _dims(dm, **kw):
     dict(qlen=0), dict(num_heads=0), dict(dcp=0), dict(interleave=0), dict(interleave=32),
     dict(interleave=3), dict(block_size=0), dict(max_local_len=-1), dict(max_blocks_per_seq=2),
     dict(num_blocks=0), dict(num_splits=0), dict(batch=-1), dict(causal=2),
+    dict(base_splits=-1), dict(base_splits=3),
 ])
 def test_invalid_dims_rejected_before_launch(dm, bad):
     d = _dims(dm, **{k: v for k, v in bad.items() if k != "causal"})
@@ -72,6 +73,26 @@ def test_invalid_dims_rejected_before_launch(dm, bad):
         dm.dcp_mla_check_dims(d)
     assert ei.value.code == dm.DCP_ERR_INVALID_ARG
     assert dm.dcp_last_error()
+
+
+def test_base_splits_range(dm):
+    # 0 and num_splits both mean "no balancing"; anything between turns it on
+    for base in (0, 1, 2):
+        dm.dcp_mla_check_dims(_dims(dm, num_splits=2, base_splits=base))
+    # balancing reads every (rank, sequence) pair's length in each metadata CTA
+    d = _dims(dm, batch=1 << 14, dcp=8, num_splits=2, base_splits=1)
+    with pytest.raises(dm.DcpError) as ei:
+        dm.dcp_mla_check_dims(d)
+    assert ei.value.code == dm.DCP_ERR_UNSUPPORTED
+
+
+def test_concurrent_items_without_a_device(dm):
+    import torch
+
+    if torch.cuda.is_available():
+        assert dm.dcp_mla_concurrent_items() >= 1
+    else:
+        assert dm.dcp_mla_concurrent_items() == -1
 
 
 def test_rank_range_checked(dm):
@@ -141,10 +162,11 @@ def test_a2a_chunk_words_and_argument_checks(dm):
 
 
 def test_workspace_size(dm):
-    # one int32 per work item (rank, sequence, split, 128-row tile), 16-byte multiple
+    # one int32 per work item (rank, sequence, split, 128-row tile) and the count of
+    # listed items, rounded up to a 16-byte multiple
     d = _dims(dm, batch=32, qlen=5, num_heads=128, dcp=8, num_splits=1)
-    assert dm.dcp_mla_workspace_size(d, 8) == 8 * 32 * 1 * 5 * 4
+    assert dm.dcp_mla_workspace_size(d, 8) == (8 * 32 * 1 * 5 + 1) * 4 + 12
     d = _dims(dm, batch=1, qlen=3, num_heads=8, dcp=2, num_splits=3)
-    assert dm.dcp_mla_workspace_size(d, 1) == 16  # 3 items, padded
+    assert dm.dcp_mla_workspace_size(d, 1) == 16  # 3 items and the count
     lib = dm.load()
     assert lib.dcp_mla_workspace_size(ctypes.byref(d), 1, None) == dm.DCP_ERR_INVALID_ARG

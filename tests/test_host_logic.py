@@ -1,7 +1,9 @@
-"""Host-side logic of the package that needs no GPU: the static split count."""
+"""Host-side logic of the package that needs no GPU: the static split count and the
+wave-balancing plan."""
 
 import math
 
+import numpy as np
 import pytest
 
 from decode_context_mla_causal_gb300.step import choose_num_splits
@@ -95,3 +97,62 @@ def test_nvml_sampler_summary_decodes_reason_bits():
     assert out["power_w_max"] == 1100.0
     s.samples = []
     assert s.summary()["reasons"] == ["no samples"]
+
+
+def test_split_plan_of_the_workloads():
+    from decode_context_mla_causal_gb300.step import choose_split_plan
+
+    # decode: 256 items of 64 tiles leave 28 of 76 slots busy in the 4th wave; the 28
+    # shortest pairs may take up to 3 splits to fill it
+    assert choose_split_plan(32, 1, 128, 8, 4096, 64, concurrent=76) == (3, 1)
+    # spec-verify (1280 items: 64 of 76 in the last wave) and long-context (672
+    # items: 64 of 76) have nothing to balance
+    assert choose_split_plan(32, 5, 128, 8, 16384, 64, concurrent=76) == (1, 0)
+    assert choose_split_plan(4, 3, 128, 8, 131072, 64, concurrent=76) == (7, 0)
+    # short sequences are not cut below 8 tiles a piece
+    assert choose_split_plan(1, 3, 8, 2, 100, 16, concurrent=76) == (2, 0)
+
+
+def _makespan(costs, slots):
+    """List scheduling in the given order (the hardware hands each next cluster to
+    the first free slot): the finish time of the last item."""
+    import heapq
+
+    free = [0.0] * slots
+    heapq.heapify(free)
+    end = 0.0
+    for c in costs:
+        t = heapq.heappop(free) + c
+        end = max(end, t)
+        heapq.heappush(free, t)
+    return end
+
+
+def test_balanced_plan_shortens_the_decode_schedule():
+    """The decode shape (32 sequences x 8 ranks, 4096 local tokens each): with the
+    per-item cost of the split model (tiles + 11), longest first on 76 slots, the
+    balanced counts finish the step earlier than one split per pair."""
+    from tests._helpers import balanced_split_counts
+
+    seq = np.full(32, 32768)
+    kw = dict(batch=32, qlen=1, num_heads=128, dcp=8, interleave=1, max_local_len=4096)
+    n = balanced_split_counts(seq, num_splits=3, base_splits=1, concurrent=76, **kw)
+    assert sorted(np.unique(n).tolist()) == [1, 2, 3]
+    assert int((n == 1).sum()) == 228 and int(n.sum()) == 228 + 76
+    costs = sorted((64 / k + 11.0 for k in n.reshape(-1) for _ in range(k)), reverse=True)
+    plain = _makespan([64 + 11.0] * 256, 76)
+    balanced = _makespan(costs, 76)
+    assert plain == pytest.approx(4 * 75.0)
+    assert balanced < 0.9 * plain
+
+
+def test_balanced_plan_keeps_uneven_batches_whole():
+    """Lengths that already spread over the waves (spec-verify's log-uniform mix) or
+    a last wave more than half full: every pair keeps base_splits."""
+    from tests._helpers import balanced_split_counts
+
+    rng = np.random.default_rng(3)
+    seq = rng.integers(8192, 131072, size=32)
+    kw = dict(batch=32, qlen=5, num_heads=128, dcp=8, interleave=1, max_local_len=16384)
+    n = balanced_split_counts(seq, num_splits=2, base_splits=1, concurrent=76, **kw)
+    assert (n == 1).all()
