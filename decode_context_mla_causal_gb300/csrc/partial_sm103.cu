@@ -72,6 +72,8 @@
 //
 // Work items reach clusters longest first (order_kernel, below), so that items of
 // very different lengths finish together.
+#include <climits>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -235,12 +237,14 @@ struct Item {
   int k, b, s, t;
   int qr0, rows_valid;
   int t_start, t_end, n_tiles;
+  bool bad_split;  // the split bounds were outside [0, MP] (the item then covers nothing)
 };
 
 // Work item `item` (natural order: rank, sequence, split, row tile, the row tile
 // fastest) with its tile range.
 __device__ __forceinline__ Item decode_item(const Params& p, int item) {
   Item it;
+  it.bad_split = false;
   int rest = item;
   it.t = rest % p.n_row_tiles;
   rest /= p.n_row_tiles;
@@ -259,7 +263,10 @@ __device__ __forceinline__ Item decode_item(const Params& p, int item) {
     maxL = max(maxL, p.row_len[(int64_t)it.k * R + (int64_t)it.b * p.qlen + j]);
   const int64_t sb = ((int64_t)it.k * p.batch + it.b) * p.num_splits + it.s;
   int beg = p.split_beg[sb], end = p.split_end[sb];
-  if (beg < 0 || end < beg || end > p.max_pages) beg = end = 0;  // status raised once below
+  if (beg < 0 || end < beg || end > p.max_pages) {  // the status is raised once, by the kernel
+    it.bad_split = true;
+    beg = end = 0;
+  }
   it.t_start = beg * p.subpage;
   it.t_end = min(end * p.subpage, maxL);
   it.n_tiles = it.t_end > it.t_start ? (it.t_end - it.t_start + kTileN - 1) / kTileN : 0;
@@ -544,36 +551,50 @@ __device__ __noinline__ void rescale_o(uint32_t tO, float a) {
 // shared-memory slice of this warp (chunk c of row r at 16-byte position c ^ (r mod 8)),
 // then lane l stores chunk (l mod 8) of rows 4k + l/8, k = 0..7, so one instruction
 // writes four whole 128-byte row segments (a store per thread of its own row would
-// touch 32 rows per instruction). Rows at or past rows_left are not written.
-__device__ __noinline__ void store_o(uint32_t tO, bool have_o, int rows_left, float inv,
-                                     float* dst0, uint4* slice) {
+// touch 32 rows per instruction). Rows at or past rows_left are not written. The next
+// 32 columns' tensor-memory load is in flight while the current ones are stored.
+__device__ __forceinline__ void store_o_cols(const uint32_t (&o)[32], int c4, int rows_left,
+                                             float inv, float* dst0, uint4* slice) {
   const int lane = threadIdx.x & 31;
   const int rsub = lane >> 3, chunk = lane & 7;
-  for (int c4 = 0; c4 < 4; ++c4) {
-    uint32_t o[32];
-    if (have_o) {
-      tmem_ld32(tO + 32 * c4, o);
-      tmem_wait_ld(o);
-    } else {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = 0u;
-    }
+  for (int c = 0; c < 8; ++c)
+    slice[lane * 8 + (c ^ (lane & 7))] =
+        make_uint4(__float_as_uint(__uint_as_float(o[4 * c]) * inv),
+                   __float_as_uint(__uint_as_float(o[4 * c + 1]) * inv),
+                   __float_as_uint(__uint_as_float(o[4 * c + 2]) * inv),
+                   __float_as_uint(__uint_as_float(o[4 * c + 3]) * inv));
+  __syncwarp();
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-      slice[lane * 8 + (c ^ (lane & 7))] =
-          make_uint4(__float_as_uint(__uint_as_float(o[4 * c]) * inv),
-                     __float_as_uint(__uint_as_float(o[4 * c + 1]) * inv),
-                     __float_as_uint(__uint_as_float(o[4 * c + 2]) * inv),
-                     __float_as_uint(__uint_as_float(o[4 * c + 3]) * inv));
-    __syncwarp();
+  for (int k = 0; k < 8; ++k) {
+    const int row = 4 * k + rsub;
+    if (row < rows_left)
+      *reinterpret_cast<uint4*>(dst0 + (int64_t)row * kDv + 32 * c4 + 4 * chunk) =
+          slice[row * 8 + (chunk ^ (row & 7))];
+  }
+  __syncwarp();  // the slice is written again for the next 32 columns
+}
+
+__device__ __noinline__ void store_o(uint32_t tO, bool have_o, int rows_left, float inv,
+                                     float* dst0, uint4* slice) {
+  uint32_t oa[32], ob[32];
+  if (have_o) {
+    tmem_ld32(tO, oa);
+    tmem_wait_ld(oa);
+    tmem_ld32(tO + 32, ob);
+    store_o_cols(oa, 0, rows_left, inv, dst0, slice);
+    tmem_wait_ld(ob);
+    tmem_ld32(tO + 64, oa);
+    store_o_cols(ob, 1, rows_left, inv, dst0, slice);
+    tmem_wait_ld(oa);
+    tmem_ld32(tO + 96, ob);
+    store_o_cols(oa, 2, rows_left, inv, dst0, slice);
+    tmem_wait_ld(ob);
+    store_o_cols(ob, 3, rows_left, inv, dst0, slice);
+  } else {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int row = 4 * k + rsub;
-      if (row < rows_left)
-        *reinterpret_cast<uint4*>(dst0 + (int64_t)row * kDv + 32 * c4 + 4 * chunk) =
-            slice[row * 8 + (chunk ^ (row & 7))];
-    }
-    __syncwarp();  // the slice is written again for the next 32 columns
+    for (int e = 0; e < 32; ++e) oa[e] = 0u;
+    for (int c4 = 0; c4 < 4; ++c4) store_o_cols(oa, c4, rows_left, inv, dst0, slice);
   }
 }
 
@@ -769,6 +790,7 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.bars[kBarQFull]);
   }
+  cluster_wait();  // the peer's barriers are initialised before this warp's first send
 
   const uint32_t peer = cta ^ 1;
   const uint32_t xch_local = smem_u32(sh.xch);
@@ -1097,11 +1119,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
   const int cta = (int)cluster_ctarank();
   const int cluster_id = blockIdx.x >> 1;
-  // clusters past the listed items have nothing to do (both CTAs of a cluster agree,
-  // and neither has touched a barrier or tensor memory yet)
-  if (p.n_live != nullptr && cluster_id >= *p.n_live) return;
-  const Item it = decode_item(p, p.item_order ? p.item_order[cluster_id] : cluster_id);
+  // the listed count and this cluster's entry are read together (the entry is in
+  // bounds either way); clusters past the listed items have nothing to do (both CTAs
+  // of a cluster agree, and neither has touched a barrier or tensor memory yet)
+  const int n_live = p.n_live != nullptr ? *p.n_live : INT_MAX;
+  const int item = p.item_order != nullptr ? p.item_order[cluster_id] : cluster_id;
+  if (cluster_id >= n_live) return;
 
+  // barriers and tensor memory while the item's metadata loads are in flight
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sh.bars[kBarKvFull + i], 128);
@@ -1123,18 +1148,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&sh.bars[kBarDrainP], 1);
     *sh.abort_flag = 0;
     fence_mbarrier_init_cluster();
-    const int64_t sb = ((int64_t)it.k * p.batch + it.b) * p.num_splits + it.s;
-    const int beg = p.split_beg[sb], end = p.split_end[sb];
-    if (cta == 0 && it.t == 0 && (beg < 0 || end < beg || end > p.max_pages))
-      raise_status(p.status, DCP_STATUS_BAD_SPLIT);
   }
   if (warp == kMmaWarpS) {
     tmem_alloc(sh.tmem_slot, kTmemCols);
     tmem_relinquish();
   }
+  const Item it = decode_item(p, item);
+  if (tid == 0 && cta == 0 && it.t == 0 && it.bad_split) raise_status(p.status, DCP_STATUS_BAD_SPLIT);
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();
+  // this CTA's barriers are ready for the peer. A thread waits for the peer's only where
+  // it first needs them: the softmax warps before their first send (their q load runs
+  // meanwhile), every other warp here
+  cluster_arrive();
+  if (warp >= kSoftWarps) cluster_wait();
   tc_fence_after();
   const uint32_t tbase = __shfl_sync(0xffffffffu, *sh.tmem_slot, 0);
 
