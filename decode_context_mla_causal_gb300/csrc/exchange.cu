@@ -28,11 +28,10 @@
 //                       row) entry of packed send buffers: D[128][P] =
 //                       A[128][512] . W_V[h]^T on the tensor cores (tcgen05, M = 128,
 //                       N = P, K = 512 in 8 chunks of 64, fp32 accumulator in tensor
-//                       memory). Each thread copies its vector's 128 bytes of the
-//                       chunk into the 128-byte-swizzled K-major A tile (the next
-//                       chunk's loads are in flight meanwhile); W_V rows go to the B
-//                       tile. Two stages: the stores of chunk c overlap the MMAs of
-//                       chunk c-1. The epilogue reads D back (tcgen05.ld), rounds to
+//                       memory). The threads copy the chunk's A rows and W_V rows
+//                       into 128-byte-swizzled K-major tiles with coalesced loads
+//                       (the next chunk's loads are in flight meanwhile). Two
+//                       stages: the stores of chunk c overlap the MMAs of chunk c-1. The epilogue reads D back (tcgen05.ld), rounds to
 //                       BF16 and writes the projected entries; the LSE words are
 //                       copied.
 #include <cuda_bf16.h>
@@ -413,7 +412,6 @@ a2a_project_kernel(int R, int H, int G, int num_ranks, int P, int64_t cw_in, int
   const int k = valid ? v / R : 0, row = valid ? v % R : 0;
   const int64_t entry = (int64_t)row * Hg + hl;
   const uint16_t* in_chunk = send_in + ((int64_t)k * G + d) * cw_in;
-  const uint4* arow = reinterpret_cast<const uint4*>(in_chunk + entry * kDv);
 
   if (tid == 0) {
     mbar_init(&bars[0], 1);
@@ -432,17 +430,32 @@ a2a_project_kernel(int R, int H, int G, int num_ranks, int P, int64_t cw_in, int
   const uint32_t tbase = __shfl_sync(0xffffffffu, *tslot, 0);
   const uint32_t idesc = idesc_f16(kProjVecs, P, true, false);
   const uint32_t sbase = smem_u32(base);
-  uint4 cur[8];
+  // Loads are coalesced: in every chunk, thread tid moves 16-byte piece j = tid % 8 of
+  // A rows 16i + tid / 8 (i = 0..7) and of W_V rows 16i + tid / 8 (i < P / 16), so a
+  // warp reads four whole 128-byte row segments per instruction. One chunk ahead.
+  const int jp = tid & 7, r0 = tid >> 3;
+  const uint4* asrc[8];  // this thread's A rows (nullptr: past the last vector)
 #pragma unroll
-  for (int j = 0; j < 8; ++j) cur[j] = valid ? arow[j] : make_uint4(0, 0, 0, 0);
-  // this thread's W_V rows (p = tid, tid + 128), one chunk ahead like the A row
-  const uint4* wrow = reinterpret_cast<const uint4*>(w_v + ((int64_t)h * P + tid) * kDv);
-  uint4 bcur[2][8];
+  for (int i = 0; i < 8; ++i) {
+    const int vi = blockIdx.y * kProjVecs + 16 * i + r0;
+    asrc[i] = nullptr;
+    if (vi < num_ranks * R) {
+      const int ki = vi / R, ri = vi - ki * R;
+      asrc[i] = reinterpret_cast<const uint4*>(send_in + ((int64_t)ki * G + d) * cw_in +
+                                               ((int64_t)ri * Hg + hl) * kDv) + jp;
+    }
+  }
+  const uint4* wsrc = reinterpret_cast<const uint4*>(w_v + ((int64_t)h * P + r0) * kDv) + jp;
+  const int nb = P / 16;  // W_V rows per thread
+  uint4 cur[8], bcur[16];
+  auto fetch = [&](int c) {
 #pragma unroll
-  for (int q = 0; q < 2; ++q)
+    for (int i = 0; i < 8; ++i) cur[i] = asrc[i] ? asrc[i][c * 8] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      bcur[q][j] = tid + 128 * q < P ? wrow[q * 128 * (kDv / 8) + j] : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 16; ++i)
+      if (i < nb) bcur[i] = wsrc[(int64_t)16 * i * (kDv / 8) + c * 8];
+  };
+  fetch(0);
 
   for (int c = 0; c < kDv / kProjChunk; ++c) {
     const int st = c & 1;
@@ -455,32 +468,18 @@ a2a_project_kernel(int R, int H, int G, int num_ranks, int P, int64_t cw_in, int
       __syncthreads();
       if (*abort_flag) break;
     }
-    // A row tid: the chunk's 8 groups of 8 dims, group j at 16-byte slot j ^ (tid & 7)
+    // row r of a tile: the chunk's 8 groups of 8 dims, group j at 16-byte slot j ^ (r & 7)
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<uint4*>(A + tid * 128 + ((j ^ (tid & 7)) << 4)) = cur[j];
-    if (c + 1 < kDv / kProjChunk) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) cur[j] = valid ? arow[(c + 1) * 8 + j] : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 8; ++i) {
+      const int r = 16 * i + r0;
+      *reinterpret_cast<uint4*>(A + r * 128 + ((jp ^ (r & 7)) << 4)) = cur[i];
     }
-    // B rows: the chunk's 64 weights of each projected value p
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int pr = tid + 128 * q;
-      if (pr < P) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint4*>(B + pr * 128 + ((j ^ (pr & 7)) << 4)) = bcur[q][j];
-      }
+    for (int i = 0; i < 16; ++i) {
+      const int r = 16 * i + r0;
+      if (i < nb) *reinterpret_cast<uint4*>(B + r * 128 + ((jp ^ (r & 7)) << 4)) = bcur[i];
     }
-    if (c + 1 < kDv / kProjChunk) {
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          bcur[q][j] = tid + 128 * q < P ? wrow[q * 128 * (kDv / 8) + (c + 1) * 8 + j]
-                                         : make_uint4(0, 0, 0, 0);
-    }
+    if (c + 1 < kDv / kProjChunk) fetch(c + 1);
     fence_proxy_async_smem();  // the tensor core reads the tiles (async proxy)
     tc_fence_before();
     __syncthreads();
