@@ -680,6 +680,7 @@ def main():
                                        "merge": 1e3 * sum(ct["merge"]) / K},
                          "roofline": {"bound": "tensor", "achieved": ach, "peak": tp,
                                       "unit": "TFLOP/s", "frac": ach / tp,
+                                      "traffic": profiled_traffic("partial", cfg),
                                       "step_frac": croof / cms,
                                       "hbm_frac_of_partial":
                                           cby / (cpart / 1e3) / (hp * 1e9)},
