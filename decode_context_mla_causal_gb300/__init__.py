@@ -12,7 +12,7 @@ from .binding import (  # noqa: F401
     STATUS_TIMEOUT, STATUS_BAD_SPLIT, KV_BF16, KV_FP8_E4M3, QK_DIM, V_DIM,
     DcpError, Dims, load, library_path,
     dcp_mla_subpage_size, dcp_mla_max_pages, dcp_mla_check_dims, dcp_mla_concurrent_items,
-    dcp_mla_metadata, dcp_mla_partial, dcp_mla_partial_packed, dcp_mla_workspace_size, dcp_lse_merge, dcp_last_error, dcp_mla_verify_noalloc,
+    dcp_mla_metadata, dcp_mla_partial, dcp_mla_partial_hold_q, dcp_mla_partial_packed, dcp_mla_workspace_size, dcp_lse_merge, dcp_last_error, dcp_mla_verify_noalloc,
     dcp_kv_slot_mapping, dcp_kv_write, dcp_a2a_chunk_words, dcp_a2a_pack, dcp_a2a_project,
     dcp_a2a_combine,
 )

@@ -86,6 +86,8 @@ def load() -> ctypes.CDLL:
         "dcp_mla_metadata": (I, [D, P, P, I, I, P, P, P, P, P, P]),
         "dcp_mla_partial": (I, [D, P, P, I, P, ctypes.c_float, I, I, P, P, P, P, P, P, P, P, P,
                                 P]),
+        "dcp_mla_partial_hold_q": (I, [D, P, P, I, P, ctypes.c_float, I, I, P, P, P, P, P, P, P,
+                                       P, P, ctypes.c_uint64, P]),
         "dcp_mla_workspace_size": (I, [D, I, ctypes.POINTER(ctypes.c_size_t)]),
         "dcp_lse_merge": (I, [D, I, P, P, P, P, P, P, P, P]),
         "dcp_mla_verify_noalloc": (I, [D, P, P, P, P, I, P, ctypes.c_float, P, P, P, P]),
@@ -213,6 +215,34 @@ def dcp_mla_partial(dims, q, kv, kv_dtype, kv_scale, softmax_scale, rank_begin, 
         _ptr(part_l, f32, num_ranks * NS * R * H, "part_l"),
         _ptr(workspace, None, None, "workspace", allow_none=True),
         _ptr(status, i32, 1, "status"), _stream(stream)))
+
+
+def dcp_mla_partial_hold_q(dims, q, kv, kv_dtype, kv_scale, softmax_scale, rank_begin,
+                           num_ranks, row_len, page_ids, split_beg, split_end, part_o, part_m,
+                           part_l, status, q_wait_ns, stream=None, workspace=None):
+    """dcp_mla_partial with the q arrival withheld (the failure path's test): the wait
+    for q runs out after ``q_wait_ns`` and DCP_STATUS_TIMEOUT is raised."""
+    lib = load()
+    B, R, H, NS = dims.batch, dims.rows, dims.num_heads, dims.num_splits
+    MP = lib.dcp_mla_max_pages(ctypes.byref(dims))
+    i32 = torch.int32
+    f32 = torch.float32
+    kv_elem = torch.uint8 if kv_dtype == KV_FP8_E4M3 else torch.bfloat16
+    pool = dims.num_blocks * dims.block_size * QK_DIM
+    _check(lib.dcp_mla_partial_hold_q(
+        ctypes.byref(dims), _ptr(q, torch.bfloat16, R * H * QK_DIM, "q"),
+        _ptr(kv, kv_elem, num_ranks * pool, "kv"), int(kv_dtype),
+        _ptr(kv_scale, f32, 1, "kv_scale", allow_none=True), float(softmax_scale),
+        rank_begin, num_ranks,
+        _ptr(row_len, i32, num_ranks * R, "row_len"),
+        _ptr(page_ids, i32, num_ranks * B * max(MP, 0), "page_ids"),
+        _ptr(split_beg, i32, num_ranks * B * NS, "split_beg"),
+        _ptr(split_end, i32, num_ranks * B * NS, "split_end"),
+        _ptr(part_o, f32, num_ranks * NS * R * H * V_DIM, "part_o"),
+        _ptr(part_m, f32, num_ranks * NS * R * H, "part_m"),
+        _ptr(part_l, f32, num_ranks * NS * R * H, "part_l"),
+        _ptr(workspace, None, None, "workspace", allow_none=True),
+        _ptr(status, i32, 1, "status"), int(q_wait_ns), _stream(stream)))
 
 
 def dcp_mla_partial_packed(dims, q, kv, kv_dtype, kv_scale, softmax_scale, rank_begin,

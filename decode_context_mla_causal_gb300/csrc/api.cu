@@ -118,13 +118,13 @@ dcp_status dcp_mla_metadata(const dcp_mla_dims* dims, const int32_t* seq_lens,
                   "dcp_mla_metadata");
 }
 
-dcp_status dcp_mla_partial(const dcp_mla_dims* dims, const void* q, const void* kv,
-                           dcp_kv_dtype kv_dtype, const float* kv_scale, float softmax_scale,
-                           int32_t rank_begin, int32_t num_ranks, const int32_t* row_len,
-                           const int32_t* page_ids, const int32_t* split_beg,
-                           const int32_t* split_end, float* part_o, float* part_m,
-                           float* part_l, void* workspace, uint32_t* status,
-                           dcp_stream_t stream) {
+static dcp_status partial_call(const dcp_mla_dims* dims, const void* q, const void* kv,
+                               dcp_kv_dtype kv_dtype, const float* kv_scale, float softmax_scale,
+                               int32_t rank_begin, int32_t num_ranks, const int32_t* row_len,
+                               const int32_t* page_ids, const int32_t* split_beg,
+                               const int32_t* split_end, float* part_o, float* part_m,
+                               float* part_l, void* workspace, uint32_t* status,
+                               dcp_stream_t stream, uint64_t hold_q_ns, const char* what) {
   dcp_status s = check(dims, rank_begin, num_ranks);
   if (s != DCP_OK) return s;
   if (kv_dtype != DCP_KV_BF16 && kv_dtype != DCP_KV_FP8_E4M3)
@@ -134,15 +134,42 @@ dcp_status dcp_mla_partial(const dcp_mla_dims* dims, const void* q, const void* 
   if (dims->batch == 0) return DCP_OK;
   if (!q || !kv || !row_len || !page_ids || !split_beg || !split_end || !part_o || !part_m ||
       !part_l || !status)
-    return fail(DCP_ERR_INVALID_ARG, "dcp_mla_partial: a required pointer is NULL");
+    return fail(DCP_ERR_INVALID_ARG, "%s: a required pointer is NULL", what);
   if (((uintptr_t)q & 15) || ((uintptr_t)kv & 15) || ((uintptr_t)part_o & 15) ||
       ((uintptr_t)workspace & 15))
     return fail(DCP_ERR_INVALID_ARG, "q, kv, part_o and workspace must be 16-byte aligned");
   Derived x = derive(*dims);
   return launched(launch_partial(*dims, x, q, kv, kv_dtype, kv_scale, softmax_scale, num_ranks,
                                  row_len, page_ids, split_beg, split_end, part_o, part_m, part_l,
-                                 workspace, status, (cudaStream_t)stream),
-                  "dcp_mla_partial");
+                                 workspace, status, (cudaStream_t)stream, nullptr, hold_q_ns),
+                  what);
+}
+
+dcp_status dcp_mla_partial(const dcp_mla_dims* dims, const void* q, const void* kv,
+                           dcp_kv_dtype kv_dtype, const float* kv_scale, float softmax_scale,
+                           int32_t rank_begin, int32_t num_ranks, const int32_t* row_len,
+                           const int32_t* page_ids, const int32_t* split_beg,
+                           const int32_t* split_end, float* part_o, float* part_m,
+                           float* part_l, void* workspace, uint32_t* status,
+                           dcp_stream_t stream) {
+  return partial_call(dims, q, kv, kv_dtype, kv_scale, softmax_scale, rank_begin, num_ranks,
+                      row_len, page_ids, split_beg, split_end, part_o, part_m, part_l, workspace,
+                      status, stream, 0, "dcp_mla_partial");
+}
+
+dcp_status dcp_mla_partial_hold_q(const dcp_mla_dims* dims, const void* q, const void* kv,
+                                  dcp_kv_dtype kv_dtype, const float* kv_scale,
+                                  float softmax_scale, int32_t rank_begin, int32_t num_ranks,
+                                  const int32_t* row_len, const int32_t* page_ids,
+                                  const int32_t* split_beg, const int32_t* split_end,
+                                  float* part_o, float* part_m, float* part_l, void* workspace,
+                                  uint32_t* status, uint64_t q_wait_ns, dcp_stream_t stream) {
+  if (q_wait_ns == 0 || q_wait_ns > 4000000000ull)
+    return fail(DCP_ERR_INVALID_ARG, "q_wait_ns must be in (0, 4e9] (got %llu)",
+                (unsigned long long)q_wait_ns);
+  return partial_call(dims, q, kv, kv_dtype, kv_scale, softmax_scale, rank_begin, num_ranks,
+                      row_len, page_ids, split_beg, split_end, part_o, part_m, part_l, workspace,
+                      status, stream, q_wait_ns, "dcp_mla_partial_hold_q");
 }
 
 dcp_status dcp_mla_partial_packed(const dcp_mla_dims* dims, const void* q, const void* kv,

@@ -36,7 +36,8 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
                            const int32_t* page_ids, const int32_t* split_beg,
                            const int32_t* split_end, float* part_o, float* part_m,
                            float* part_l, void* workspace, uint32_t* status,
-                           cudaStream_t stream, void* send = nullptr);
+                           cudaStream_t stream, void* send = nullptr,
+                           uint64_t hold_q_ns = 0);
 
 // Device workspace launch_partial uses for the item order (bytes, 16-byte multiple).
 size_t partial_workspace_bytes(const dcp_mla_dims& d, int num_ranks);

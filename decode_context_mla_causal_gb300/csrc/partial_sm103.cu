@@ -168,6 +168,11 @@ struct Params {
   float softmax_scale;
   int batch, qlen, H, num_splits, subpage, max_pages, n_row_tiles;
   int64_t pool_rows;  // rows of one rank's pool: num_blocks * block_size
+  // The failure path's test: hold_q = 1 withholds the softmax warps' arrivals on the q
+  // barrier, so the score issuer's wait for q runs out after q_wait_ns and the kernel
+  // stops in order (DCP_STATUS_TIMEOUT). 0 and the 4 s limit in every other call.
+  int hold_q;
+  uint64_t q_wait_ns;
 };
 
 struct Shared {
@@ -203,16 +208,17 @@ __device__ __forceinline__ Shared carve(unsigned char* raw) {
 // suspend-time hint, while a waiter that has to sleep notices the completion
 // ~170 cycles after the arrive with the hint and ~280 without. So the first
 // check is a plain try_wait, and the slow path repeats hinted try_waits; between
-// them it checks the abort flag and gives up after kTimeoutNs (raising the abort
+// them it checks the abort flag and gives up after limit_ns (raising the abort
 // flag and DCP_STATUS_TIMEOUT).
 __device__ __noinline__ bool wait_phase_slow(uint32_t a, uint32_t parity, int* abort_flag,
-                                             uint32_t* status, bool cluster_acquire) {
+                                             uint32_t* status, bool cluster_acquire,
+                                             uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (cluster_acquire ? mbar_wait_sleep_cluster(a, parity) : mbar_wait_sleep(a, parity))
       return true;
     if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
-    if (globaltimer_ns() - t0 > kTimeoutNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *reinterpret_cast<volatile int*>(abort_flag) = 1;
       raise_status(status, DCP_STATUS_TIMEOUT);
       return false;
@@ -220,17 +226,18 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t a, uint32_t parity, int* a
   }
 }
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, int* abort_flag,
-                                           uint32_t* status, bool cluster_acquire) {
+                                           uint32_t* status, bool cluster_acquire,
+                                           uint64_t limit_ns = kTimeoutNs) {
   const uint32_t a = smem_u32(bar);
   if (cluster_acquire ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
-  return wait_phase_slow(a, parity, abort_flag, status, cluster_acquire);
+  return wait_phase_slow(a, parity, abort_flag, status, cluster_acquire, limit_ns);
 }
 
 // wait_phase for a whole converged warp, with a warp-uniform result (the
 // elect.sync of the tcgen05 issue that follows needs every lane).
 __device__ __forceinline__ bool wait_uniform(uint64_t* bar, uint32_t parity, int* abort_flag,
-                                             uint32_t* status) {
-  return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, status, false));
+                                             uint32_t* status, uint64_t limit_ns = kTimeoutNs) {
+  return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, status, false, limit_ns));
 }
 
 struct Item {
@@ -471,7 +478,7 @@ __device__ __forceinline__ void run_score_chain(const Params& p, const Shared& s
                                                 uint32_t tbase) {
   constexpr uint32_t idq = idesc_f16(kRows, kTileN, !kFp8, false);
   const uint32_t stage0 = smem_u32(sh.stages);
-  if (wait_uniform(&sh.bars[kBarQFull], 0, sh.abort_flag, p.status)) {
+  if (wait_uniform(&sh.bars[kBarQFull], 0, sh.abort_flag, p.status, p.q_wait_ns)) {
     tc_fence_after();
     for (int i = 0; i < it.n_tiles; ++i) {
       const int st = i % kStages;
@@ -788,7 +795,7 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
     tc_fence_before();
     if (q_range) raise_status(p.status, DCP_STATUS_Q_RANGE);
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.bars[kBarQFull]);
+    if (lane == 0 && !p.hold_q) mbar_arrive(&sh.bars[kBarQFull]);
   }
   cluster_wait();  // the peer's barriers are initialised before this warp's first send
 
@@ -1195,7 +1202,7 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
                            const int32_t* page_ids, const int32_t* split_beg,
                            const int32_t* split_end, float* part_o, float* part_m,
                            float* part_l, void* workspace, uint32_t* status,
-                           cudaStream_t stream, void* send) {
+                           cudaStream_t stream, void* send, uint64_t hold_q_ns) {
   Params p;
   p.q = reinterpret_cast<const uint16_t*>(q);
   p.kv = reinterpret_cast<const uint8_t*>(kv);
@@ -1210,6 +1217,8 @@ cudaError_t launch_partial(const dcp_mla_dims& d, const Derived& x, const void* 
   p.status = status;
   p.item_order = nullptr;
   p.n_live = nullptr;
+  p.hold_q = hold_q_ns > 0 ? 1 : 0;
+  p.q_wait_ns = hold_q_ns > 0 ? hold_q_ns : kTimeoutNs;
   p.send = reinterpret_cast<uint16_t*>(send);
   p.G = d.dcp;
   p.send_cw = send ? a2a_chunk_words(d.batch * d.qlen, d.num_heads / d.dcp, kDv) : 0;

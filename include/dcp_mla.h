@@ -217,6 +217,24 @@ dcp_status dcp_mla_partial(const dcp_mla_dims* dims, const void* q, const void* 
                            float* part_l, void* workspace, uint32_t* status,
                            dcp_stream_t stream);
 
+/*
+ * Test of the failure path of dcp_mla_partial (same arguments and checks): the
+ * softmax warps withhold their arrivals on the barrier that tells the score issuer
+ * the q tile is in tensor memory, so the issuer's bounded wait runs out after
+ * q_wait_ns (in (0, 4e9]) instead of 4 s. Every work item then stops in order:
+ * DCP_STATUS_TIMEOUT is ORed into *status, every role leaves its loop, in-flight
+ * tensor-core work is drained and tensor memory freed; the partial outputs are
+ * not meaningful. No wait is unbounded, nothing traps, and the context stays
+ * usable for the next call.
+ */
+dcp_status dcp_mla_partial_hold_q(const dcp_mla_dims* dims, const void* q, const void* kv,
+                                  dcp_kv_dtype kv_dtype, const float* kv_scale,
+                                  float softmax_scale, int32_t rank_begin, int32_t num_ranks,
+                                  const int32_t* row_len, const int32_t* page_ids,
+                                  const int32_t* split_beg, const int32_t* split_end,
+                                  float* part_o, float* part_m, float* part_l, void* workspace,
+                                  uint32_t* status, uint64_t q_wait_ns, dcp_stream_t stream);
+
 /* Bytes of device workspace dcp_mla_partial takes for these dims and num_ranks. */
 dcp_status dcp_mla_workspace_size(const dcp_mla_dims* dims, int32_t num_ranks, size_t* bytes);
 
