@@ -34,29 +34,33 @@
 //     55 (N=64) to 130 (N=256) cycles; branches or arithmetic between them were
 //     measured to double that. The whole q.k contraction is one straight-line
 //     chain (q from tensor memory), and P.V has its own issuing thread.
-//   * The factor exchange runs one tile behind: iteration i loads the scores of
-//     tile i and sends its factors, then finishes tile i-1 with the factors the
-//     peer sent an iteration earlier, so the exchange latency overlaps work.
-//     P.V starts as soon as P is written, so the next P write (one iteration
-//     later) rarely waits for it.
+//   * The per-tile softmax work is split in two stages on different warps. The front
+//     warps turn the scores of tile i into factors and send them; they keep no state
+//     across tiles (the factors are relative to the half's own maximum). The back
+//     warps then finish tile i with the peer's factors: the running reference, P,
+//     and l. So the exchange latency and the front of the next tile overlap the back
+//     of the current one, and the front runs up to two tiles ahead (the exchange and
+//     own-factor buffers are double-buffered). P.V starts as soon as P is written.
 //
-// Per CTA (448 threads):
-//   warps 0-7   softmax: warp w owns rows 32*(w%4) .. +31 (TMEM lane quarter)
-//               and token half w/4 of every 64-token tile; Q into TMEM, factor
-//               exchange (double-buffered slots), lazy online softmax, P (16-bit)
-//               into TMEM, epilogue for O columns [128*(w/4), +128). The partner
-//               warp's half maximum comes through shared memory. Its arrival, and the
-//               completion of the previous tile's P.V, are on the same barrier that the
-//               peer's factors complete, so one wait covers all three. A thread keeps
-//               its own f16 factors of the last two tiles in shared memory.
-//   warps 8-11  KV producers: 16-byte loads of the paged cache rows (subpage ids
+// Per CTA (704 threads; 80 registers each: the six warps of a sub-partition share its
+// 16K registers):
+//   warps 0-7   front: warp w owns rows 32*(w%4) .. +31 (TMEM lane quarter) and token
+//               half w/4 of every 64-token tile; Q into TMEM at the start; S -> own
+//               f16 factors and the half maximum -> the peer's exchange slot
+//               (st.async) and the local own-factor buffer.
+//   warps 8-15  back: the same rows and halves. One wait covers the peer's factors,
+//               the local front warps' factors and maxima, and the completion of the
+//               previous tile's P.V (all are arrivals on the slot's barrier). Lazy
+//               online softmax, P (16-bit) into TMEM, l.
+//   epilogue    all 16 warps: 64 O columns each of their rows.
+//   warps 16-19 KV producers: 16-byte loads of the paged cache rows (subpage ids
 //               from the metadata, bounds-checked), FP8 E4M3 -> f16 conversion,
 //               stores into 128-byte-swizzled K-major tiles of a 3-stage ring.
 //               FP8 keeps two tiles in flight (registers + cp.async staging in
 //               shared memory), so a freed stage only waits for the conversion.
-//   warp 12     TMEM allocation; issues S = Q[tmem] . K_tile^T (M=128, N=64, all
+//   warp 20     TMEM allocation; issues S = Q[tmem] . K_tile^T (M=128, N=64, all
 //               of this CTA's dims).
-//   warp 13     issues O += P[tmem] . V_tile (M=128, N=256, V read MN-major from
+//   warp 21     issues O += P[tmem] . V_tile (M=128, N=256, V read MN-major from
 //               the same swizzled tile as K).
 //   The issuing warps run converged and one elected lane issues each tcgen05
 //   instruction, so its operands are warp-uniform values.
@@ -96,20 +100,23 @@ constexpr int kStageBytes = kMaxAtoms * kAtomBytes;
 constexpr int kXchEBytes = 2 * 4 * kRows * 16;
 constexpr int kXchSlotBytes = kXchEBytes + 2 * kRows * 4;
 constexpr int kXchSlots = 2;
-constexpr int kMOwnBufs = 3;  // own half maxima, by tile mod 3 (a warp writing tile t+3
-                              // has seen every warp's S load of tile t+2, after its read of t)
-constexpr int kMOwnBytes = kMOwnBufs * 2 * kRows * 4;   // [tile%3][half][row] f32
+constexpr int kMOwnBufs = 2;  // own half maxima, by tile mod 2 (the front warps write tile
+                              // t+2 once the back warps have finished tile t)
+constexpr int kMOwnBytes = kMOwnBufs * 2 * kRows * 4;   // [tile%2][half][row] f32
 constexpr int kLCombBytes = 2 * kRows * 4;              // [half][row] f32, epilogue
+constexpr int kEInvBytes = kRows * 4;                   // [row] f32, epilogue output scale
 constexpr int kEPrevBytes = 2 * 2 * 4 * kRows * 16;  // own f16 factors, as sent:
                                                      // [tile%2][half][group 4][row][8]
 // FP8 producer staging: each producer thread's 16-byte chunks of one tile (the
 // tile after next), [chunk][thread], written by cp.async
 constexpr int kRawBytes = kMaxAtoms * 2 * 128 * 16;
-constexpr int kSoftWarps = 8;
-constexpr int kProdWarp0 = 8;
-constexpr int kMmaWarpS = 12;
-constexpr int kMmaWarpP = 13;
-constexpr int kThreads = 14 * 32;
+constexpr int kFrontWarps = 8;   // warps 0-7: scores -> own factors -> peer
+constexpr int kBackWarps = 8;    // warps 8-15: both CTAs' factors -> P, running reference
+constexpr int kSoftWarps = kFrontWarps + kBackWarps;
+constexpr int kProdWarp0 = 16;
+constexpr int kMmaWarpS = 20;
+constexpr int kMmaWarpP = 21;
+constexpr int kThreads = 22 * 32;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr uint32_t kTmemCols = 512;
 // Lazy reference: M is raised only when the tile bound passes M + kRaiseAbove, and
@@ -135,7 +142,10 @@ enum {
                                        // the 8 local warps wrote their half maxima and the
                                        // previous tile's P.V completed
   kBarXFree = kBarXFull + kXchSlots,   // [2] count 8: the peer consumed what I wrote
-  kBarLComb = kBarXFree + kXchSlots,   // count 8: epilogue l halves written
+  kBarEFree = kBarXFree + kXchSlots,   // [2] count 8: the local back warps consumed the
+                                       // own factors and maxima of that slot
+  kBarLComb = kBarEFree + kXchSlots,   // count 8: epilogue l halves written
+  kBarEpi,                             // count 8: the output scale of every row written
   kBarDrainS,
   kBarDrainP,
   kNumBars
@@ -143,7 +153,7 @@ enum {
 
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes +
                               kXchSlots * kXchSlotBytes + kMOwnBytes + kLCombBytes +
-                              kEPrevBytes + kRawBytes + kNumBars * 8 + 16;
+                              kEInvBytes + kEPrevBytes + kRawBytes + kNumBars * 8 + 16;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct Params {
@@ -180,6 +190,7 @@ struct Shared {
   uint8_t* xch;   // kXchSlots slots
   float* mown;    // own half maxima per tile
   float* lcomb;   // epilogue l halves
+  float* einv;    // epilogue output scale per row
   uint4* eprev;   // own factors (f16, as sent) of the last two tiles
   uint8_t* raw;   // FP8 producer staging
   uint64_t* bars;
@@ -195,7 +206,8 @@ __device__ __forceinline__ Shared carve(unsigned char* raw) {
   s.xch = base + kStages * kStageBytes;
   s.mown = reinterpret_cast<float*>(s.xch + kXchSlots * kXchSlotBytes);
   s.lcomb = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s.mown) + kMOwnBytes);
-  s.eprev = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(s.lcomb) + kLCombBytes);
+  s.einv = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s.lcomb) + kLCombBytes);
+  s.eprev = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(s.einv) + kEInvBytes);
   s.raw = reinterpret_cast<uint8_t*>(s.eprev) + kEPrevBytes;
   s.bars = reinterpret_cast<uint64_t*>(s.raw + kRawBytes);
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + kNumBars);
@@ -553,13 +565,12 @@ __device__ __noinline__ void rescale_o(uint32_t tO, float a) {
   tmem_wait_st();
 }
 
-// Stores this warp's 32 rows of the normalised partial output (its 128 columns),
-// 32 columns at a time: lane r scales row r by its 1/l and writes it into a 4 KB
+// Stores 32 columns (c4-th group of the warp's columns) of this warp's 32 rows of the
+// normalised partial output: lane r scales row r by its 1/l and writes it into a 4 KB
 // shared-memory slice of this warp (chunk c of row r at 16-byte position c ^ (r mod 8)),
 // then lane l stores chunk (l mod 8) of rows 4k + l/8, k = 0..7, so one instruction
 // writes four whole 128-byte row segments (a store per thread of its own row would
-// touch 32 rows per instruction). Rows at or past rows_left are not written. The next
-// 32 columns' tensor-memory load is in flight while the current ones are stored.
+// touch 32 rows per instruction). Rows at or past rows_left are not written.
 __device__ __forceinline__ void store_o_cols(const uint32_t (&o)[32], int c4, int rows_left,
                                              float inv, float* dst0, uint4* slice) {
   const int lane = threadIdx.x & 31;
@@ -582,34 +593,32 @@ __device__ __forceinline__ void store_o_cols(const uint32_t (&o)[32], int c4, in
   __syncwarp();  // the slice is written again for the next 32 columns
 }
 
+// This warp's 64 output columns of its 32 rows (two passes of store_o_cols). The
+// second pass's tensor-memory load is in flight while the first is stored.
 __device__ __noinline__ void store_o(uint32_t tO, bool have_o, int rows_left, float inv,
                                      float* dst0, uint4* slice) {
   uint32_t oa[32], ob[32];
   if (have_o) {
     tmem_ld32(tO, oa);
-    tmem_wait_ld(oa);
     tmem_ld32(tO + 32, ob);
+    tmem_wait_ld(oa);
     store_o_cols(oa, 0, rows_left, inv, dst0, slice);
     tmem_wait_ld(ob);
-    tmem_ld32(tO + 64, oa);
     store_o_cols(ob, 1, rows_left, inv, dst0, slice);
-    tmem_wait_ld(oa);
-    tmem_ld32(tO + 96, ob);
-    store_o_cols(oa, 2, rows_left, inv, dst0, slice);
-    tmem_wait_ld(ob);
-    store_o_cols(ob, 3, rows_left, inv, dst0, slice);
   } else {
 #pragma unroll
     for (int e = 0; e < 32; ++e) oa[e] = 0u;
-    for (int c4 = 0; c4 < 4; ++c4) store_o_cols(oa, c4, rows_left, inv, dst0, slice);
+    for (int c4 = 0; c4 < 2; ++c4) store_o_cols(oa, c4, rows_left, inv, dst0, slice);
   }
 }
 
-// The packed epilogue: this warp's 32 rows of its 128 output columns, normalised
-// and rounded to BF16 (nearest even), written into the all-to-all send buffer: query
-// row qr of the tile is head qr mod H of verify row qr / H, whose entry lives in the
-// chunk for the head's destination. 64 columns at a time go through the warp's 4 KB
-// slice (as in store_o), so one instruction stores four 128-byte row segments.
+// The packed epilogue: this warp's 32 rows of its 64 output columns, normalised and
+// rounded to BF16 (nearest even), written into the all-to-all send buffer: query row
+// qr of the tile is head qr mod H of verify row qr / H, whose entry lives in the chunk
+// for the head's destination. 32 columns (64 bytes of a row) at a time go through the
+// warp's slice: lane r writes its row's four 16-byte chunks (chunk c at position
+// c ^ ((r / 2) mod 4), conflict-free), then lane l stores chunk (l mod 4) of rows
+// 8k + l/4, k = 0..3, so one instruction writes eight 64-byte row segments.
 // send_k: this rank's send buffer; cw: words per chunk; qr_first: the warp's first
 // query row; entry_row0: verify-row index of the sequence's first row (b * qlen);
 // col0: the first of the warp's output columns.
@@ -617,30 +626,26 @@ __device__ __noinline__ void store_o_packed(uint32_t tO, bool have_o, int rows_l
                                             uint4* slice, uint16_t* send_k, int64_t cw, int H,
                                             int Hg, int qr_first, int64_t entry_row0, int col0) {
   const int lane = threadIdx.x & 31;
-  const int rsub = lane >> 3, chunk = lane & 7;
-  uint16_t* dst[8];  // the send-buffer entry of each row this lane stores
+  const int rsub = lane >> 2, chunk = lane & 3;
+  uint16_t* dst[4];  // the send-buffer entry of each row this lane stores
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int qrk = qr_first + 4 * k + rsub;
+  for (int k = 0; k < 4; ++k) {
+    const int qrk = qr_first + 8 * k + rsub;
     const int jk = qrk / H, hk = qrk - jk * H;
     const int dk = hk / Hg;
     dst[k] = send_k + dk * cw + ((entry_row0 + jk) * Hg + (hk - dk * Hg)) * kDv + col0;
   }
-  for (int c8 = 0; c8 < 2; ++c8) {
-    uint32_t o[64];
+  for (int c2 = 0; c2 < 2; ++c2) {
+    uint32_t o[32];
     if (have_o) {
-      uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[0]);
-      uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[32]);
-      tmem_ld32(tO + 64 * c8, o0);
-      tmem_ld32(tO + 64 * c8 + 32, o1);
-      tmem_wait_ld(o0);
-      tmem_wait_ld(o1);
+      tmem_ld32(tO + 32 * c2, o);
+      tmem_wait_ld(o);
     } else {
 #pragma unroll
-      for (int e = 0; e < 64; ++e) o[e] = 0u;
+      for (int e = 0; e < 32; ++e) o[e] = 0u;
     }
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -648,17 +653,17 @@ __device__ __noinline__ void store_o_packed(uint32_t tO, bool have_o, int rows_l
                                                   __uint_as_float(o[8 * c + 2 * e + 1]) * inv);
         w[e] = *reinterpret_cast<uint32_t*>(&b2);
       }
-      slice[lane * 8 + (c ^ (lane & 7))] = make_uint4(w[0], w[1], w[2], w[3]);
+      slice[lane * 4 + (c ^ ((lane >> 1) & 3))] = make_uint4(w[0], w[1], w[2], w[3]);
     }
     __syncwarp();
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int row = 4 * k + rsub;
+    for (int k = 0; k < 4; ++k) {
+      const int row = 8 * k + rsub;
       if (row < rows_left)
-        *reinterpret_cast<uint4*>(dst[k] + 64 * c8 + 8 * chunk) =
-            slice[row * 8 + (chunk ^ (row & 7))];
+        *reinterpret_cast<uint4*>(dst[k] + 32 * c2 + 8 * chunk) =
+            slice[row * 4 + (chunk ^ ((row >> 1) & 3))];
     }
-    __syncwarp();  // the slice is written again for the next 64 columns
+    __syncwarp();  // the slice is written again for the next 32 columns
   }
 }
 
@@ -760,244 +765,284 @@ __device__ __forceinline__ float2 mul_f16x2_f32(uint32_t a, uint32_t b) {
   return r;
 }
 
+// Front warps (0-7): warp w owns rows 32*(w%4) .. +31 and token half w/4 of every tile.
+// Per tile: S -> own factors and half maximum -> the peer's slot and the local buffers.
+// Keeps no state across tiles (the factors are relative to the half's own maximum), so
+// it runs up to two tiles ahead of the back warps. Returns false on a timeout.
+template <bool kFp8, int kAtoms>
+__device__ __forceinline__ bool run_front(const Params& p, const Shared& sh, const Item& it,
+                                          uint32_t tbase, int lane, int qw, int h, int r,
+                                          int row_end, float sc) {
+  constexpr int cta = kAtoms - 4;
+  const uint32_t tS = tbase + ((uint32_t)(qw * 32) << 16) + kColS + 32 * h;
+  const uint32_t peer = cta ^ 1;
+  const uint32_t xch_remote = mapa_shared(smem_u32(sh.xch), peer);
+  const uint32_t xfull_remote = mapa_shared(smem_u32(&sh.bars[kBarXFull]), peer);
+  const int32_t* pages = p.page_ids + ((int64_t)it.k * p.batch + it.b) * p.max_pages;
+  const int lg_sub = __ffs(p.subpage) - 1;
+  const int64_t pool_pages = p.pool_rows >> lg_sub;
+  const bool big_pages = p.subpage >= kTileN;
+  auto wait_warp = [&](int bar, uint32_t parity, bool cluster) -> bool {
+    return __all_sync(0xffffffffu,
+                      wait_phase(&sh.bars[bar], parity, sh.abort_flag, p.status, cluster));
+  };
+  const int n = it.n_tiles;
+  // own factors (f16, the words sent to the peer) by tile mod 2: [slot][half][group 4][row]
+  uint4* eprev = sh.eprev + h * 4 * kRows + r;
+  int32_t pg_next = (big_pages && n > 0) ? __ldg(pages + (it.t_start >> lg_sub)) : 0;
+  for (int i = 0; i < n; ++i) {
+    const int tok0 = it.t_start + i * kTileN;
+    const int32_t pg_tile = pg_next;
+    if (!wait_warp(kBarSFull, i & 1, false)) return false;
+    tc_fence_after();
+    float e_cur[32];
+    {
+      uint32_t sv[32];
+      tmem_ld32(tS, sv);
+      tmem_wait_ld(sv);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) e_cur[c] = __uint_as_float(sv[c]);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.bars[kBarSFree]);
+    if (big_pages && i + 1 < n) pg_next = __ldg(pages + ((tok0 + kTileN) >> lg_sub));
+    // visible tokens of this row in this half: [tok0 + 32h, row_end), pages valid
+    const int cnt = max(0, min(32, row_end - tok0 - 32 * h));
+    const bool page_ok = !big_pages || (pg_tile >= 0 && pg_tile < pool_pages);
+    // e_cur := 2^(x*sc - m*sc + 14) with x the raw partial score (sc > 0); masked
+    // tokens (past the row's boundary, invalid pages) become -inf, i.e. factor 0
+    uint32_t vis = cnt >= 32 ? 0xFFFFFFFFu : ((1u << cnt) - 1u);
+    if (!page_ok) vis = 0;
+    if (!big_pages && vis) vis = small_page_mask(vis, pages, tok0 + 32 * h, cnt, lg_sub, pool_pages);
+    if (vis != 0xFFFFFFFFu) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) e_cur[c] = ((vis >> c) & 1u) ? e_cur[c] : -INFINITY;
+    }
+    float m4[4] = {e_cur[0], e_cur[1], e_cur[2], e_cur[3]};
+#pragma unroll
+    for (int c = 4; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], e_cur[c]);
+    const float m_cur = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sc;  // -inf: none visible
+    const float bias = m_cur == -INFINITY ? 0.f : kFactorLog2 - m_cur;
+    // x*sc + bias two at a time (packed fp32 FMA), then 2^. on the MUFU unit
+    const float2 sc2 = make_float2(sc, sc), bias2 = make_float2(bias, bias);
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+      const float2 y = __ffma2_rn(make_float2(e_cur[c], e_cur[c + 1]), sc2, bias2);
+      e_cur[c] = fast_exp2(y.x);
+      e_cur[c + 1] = fast_exp2(y.y);
+    }
+    const int slot = i & 1;
+    // slot i&1 of the local buffers is free once the back warps have finished tile i-2,
+    // and the peer's slot i&1 once the peer's back warps have
+    if (i >= 2 && !wait_warp(kBarEFree + slot, ((i >> 1) - 1) & 1, false)) return false;
+    sh.mown[(slot * 2 + h) * kRows + r] = m_cur;
+    if (i >= 2 && !wait_warp(kBarXFree + slot, ((i >> 1) - 1) & 1, true)) return false;
+    // st.async: each store completes its bytes on the peer's xfull[slot], which the
+    // peer armed with the slot size; no release fence is needed
+    const uint32_t dst = xch_remote + slot * kXchSlotBytes;
+    const uint32_t rbar = xfull_remote + 8 * slot;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t w4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __half2 hh = __floats2half2_rn(e_cur[8 * g + 2 * e], e_cur[8 * g + 2 * e + 1]);
+        w4[e] = *reinterpret_cast<uint32_t*>(&hh);
+      }
+      st_async_v4(dst + (uint32_t)(((h * 4 + g) * kRows + r) * 16), w4[0], w4[1], w4[2],
+                  w4[3], rbar);
+      eprev[(slot * 8 + g) * kRows] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+    st_async_b32(dst + kXchEBytes + (uint32_t)((h * kRows + r) * 4), __float_as_uint(m_cur),
+                 rbar);
+    // the own factors and the half maximum of tile i are in the local buffers
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.bars[kBarXFull + slot]);
+  }
+  return true;
+}
+
+// Back warps (8-15): warp w owns rows 32*(w%4) .. +31 and token half (w/4)%2. Per tile:
+// the tile bound from both CTAs' half maxima, the lazy reference M, a rescale of O when
+// M moves, P = E_own * E_peer * 2^(bound - M) into tensor memory for the P.V issuer, and
+// the half's running sum l. Returns false on a timeout.
+template <bool kFp8>
+__device__ __forceinline__ bool run_back(const Params& p, const Shared& sh, const Item& it,
+                                         uint32_t tbase, int cta, int lane, int warp, int qw,
+                                         int h, int r, float& M, float& l_half) {
+  const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+  const uint32_t tP = tbase + lane_off + kColP + 16 * h;
+  const uint32_t tO = tbase + lane_off + kColO + 128 * h;
+  const uint32_t xfree_remote = mapa_shared(smem_u32(&sh.bars[kBarXFree]), cta ^ 1);
+  auto wait_warp = [&](int bar, uint32_t parity, bool cluster) -> bool {
+    return __all_sync(0xffffffffu,
+                      wait_phase(&sh.bars[bar], parity, sh.abort_flag, p.status, cluster));
+  };
+  const bool armer = warp == kFrontWarps && lane == 0;
+  const uint4* eown = sh.eprev + h * 4 * kRows + r;
+  const int n = it.n_tiles;
+  for (int t = 0; t < n; ++t) {
+    const int slot = t & 1;
+    // one thread arms this use of the slot with its size (the bytes may already be in)
+    if (armer) {
+      mbar_arrive_expect_tx(&sh.bars[kBarXFull + slot], kXchSlotBytes);
+      if (t == 0) mbar_arrive(&sh.bars[kBarXFull + slot]);  // no P.V before tile 0
+    }
+    // the peer's factors, the local front warps' factors and maxima, the previous P.V
+    if (!wait_warp(kBarXFull + slot, (t >> 1) & 1, true)) return false;
+    const uint8_t* src = sh.xch + slot * kXchSlotBytes;
+    const float* mpeer = reinterpret_cast<const float*>(src + kXchEBytes);
+    const float* mown = sh.mown + slot * 2 * kRows;
+    // tile bound of the row: max over both halves of m_own + m_peer
+    const float mo0 = mown[r], mo1 = mown[kRows + r];
+    const float mp0 = mpeer[r], mp1 = mpeer[kRows + r];
+    const float ub0 = (mo0 == -INFINITY || mp0 == -INFINITY) ? -INFINITY : mo0 + mp0;
+    const float ub1 = (mo1 == -INFINITY || mp1 == -INFINITY) ? -INFINITY : mo1 + mp1;
+    const float ub = fmaxf(ub0, ub1);
+    const float ub_h = h ? ub1 : ub0;
+    const bool need = ub != -INFINITY && (M == -INFINITY || ub > M + kRaiseAbove);
+    float alpha = 1.f;
+    if (need) {
+      const float m_new = ub - kRefBelow;
+      alpha = M == -INFINITY ? 0.f : fast_exp2(M - m_new);
+      l_half *= alpha;
+      M = m_new;
+    }
+    // P.V(t-1) has completed (its commit was an arrival on this tile's exchange
+    // barrier): the P buffer is free and O is stable
+    tc_fence_after();
+    if (t >= 1 && __any_sync(0xffffffffu, need)) rescale_o(tO, need ? alpha : 1.f);
+    // p = E_own * E_peer * 2^(m_own + m_peer - M); both factors carry 2^14 and are the
+    // f16 words that were exchanged, so the two CTAs form bit-identical weights. 8
+    // tokens per step (two steps per loop body)
+    const float f = ub_h == -INFINITY ? 0.f : fast_exp2(ub_h - M - 2.0f * kFactorLog2);
+    const float2 f2 = make_float2(f, f);
+    float2 lsum2 = make_float2(0.f, 0.f);
+    const uint4* pe_src = reinterpret_cast<const uint4*>(src) + h * 4 * kRows + r;
+    const uint4* own = eown + slot * 8 * kRows;
+#pragma unroll 2
+    for (int g = 0; g < 4; ++g) {
+      const uint4 a = own[g * kRows], b = pe_src[g * kRows];
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // two weights at a time: the exact f32 product of the two f16 factors, times f
+        const float2 pp = __fmul2_rn(mul_f16x2_f32(aw[e], bw[e]), f2);
+        // l sums the fp32 weights; the P.V contraction uses P rounded to 16 bits
+        lsum2 = __fadd2_rn(lsum2, pp);
+        if (kFp8) {
+          __half2 hh = __floats2half2_rn(pp.x, pp.y);
+          pk[e] = *reinterpret_cast<uint32_t*>(&hh);
+        } else {
+          __nv_bfloat162 hh = __floats2bfloat162_rn(pp.x, pp.y);
+          pk[e] = *reinterpret_cast<uint32_t*>(&hh);
+        }
+      }
+      tmem_st4(tP + 4 * g, pk);
+    }
+    __syncwarp();
+    // done with the peer's slot and the local own-factor slot: the values are in
+    // registers already
+    if (lane == 0) {
+      mbar_arrive_remote_relaxed(xfree_remote + 8 * slot);
+      mbar_arrive(&sh.bars[kBarEFree + slot]);
+    }
+    l_half += lsum2.x + lsum2.y;
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.bars[kBarPFull]);
+  }
+  return true;
+}
+
+// The softmax warps: front (0-7) and back (8-15) loops, then a shared epilogue in which
+// each of the 16 warps stores 64 of the CTA's 256 output columns of its 32 rows.
 template <bool kFp8, int kAtoms>
 __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, const Item& it,
                                             uint32_t tbase, int tid, int warp) {
   constexpr int cta = kAtoms - 4;
   constexpr int d0 = 256 * cta;
   const int lane = tid & 31;
-  const int qw = warp & 3;   // TMEM lane quarter
-  const int h = warp >> 2;   // token half of each tile / O column half
+  const int qw = warp & 3;          // TMEM lane quarter
+  const int h = (warp >> 2) & 1;    // token half of each tile / O column half
+  const bool back = warp >= kFrontWarps;
   const int r = qw * 32 + lane;
-  const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-  const uint32_t tS = tbase + lane_off + kColS + 32 * h;
-  const uint32_t tP = tbase + lane_off + kColP + 16 * h;
-  const uint32_t tO = tbase + lane_off + kColO + 128 * h;
-  const uint32_t tQ = tbase + lane_off + kColQ;
   const int qrows = p.qlen * p.H;
   const int R = p.batch * p.qlen;
   const bool row_ok = r < it.rows_valid;
   const int qr = it.qr0 + r;
   const int j = row_ok ? qr / p.H : 0;
-  const int L = row_ok ? p.row_len[(int64_t)it.k * R + (int64_t)it.b * p.qlen + j] : 0;
-  const int row_end = min(L, it.t_end);  // tokens at or past it are invisible to this row
   const float kv_scale = p.kv_scale ? *p.kv_scale : 1.0f;
-  const float sc = p.softmax_scale * kv_scale * kLog2e;
-
-  {
-    // this warp's 32 rows start at row qw*32 of the tile; the own-factor buffer, first
-    // written after the first scores (which need every warp's q), lends each warp a
-    // 4 KB slice for the transpose
-    const int r_first = qw * 32;
-    const uint16_t* rows0 = p.q + ((int64_t)it.b * qrows + it.qr0 + r_first) * kDqk + d0;
-    const bool q_range = load_q<kFp8, kAtoms>(rows0, it.rows_valid - r_first, h, tQ,
-                                              sh.eprev + warp * 256);
-    tc_fence_before();
-    if (q_range) raise_status(p.status, DCP_STATUS_Q_RANGE);
-    __syncwarp();
-    if (lane == 0 && !p.hold_q) mbar_arrive(&sh.bars[kBarQFull]);
-  }
-  cluster_wait();  // the peer's barriers are initialised before this warp's first send
-
-  const uint32_t peer = cta ^ 1;
-  const uint32_t xch_local = smem_u32(sh.xch);
-  const uint32_t xch_remote = mapa_shared(xch_local, peer);
-  const uint32_t xfull_remote = mapa_shared(smem_u32(&sh.bars[kBarXFull]), peer);
-  const uint32_t xfree_remote = mapa_shared(smem_u32(&sh.bars[kBarXFree]), peer);
-  const int32_t* pages = p.page_ids + ((int64_t)it.k * p.batch + it.b) * p.max_pages;
-  const int lg_sub = __ffs(p.subpage) - 1;
-  const int64_t pool_pages = p.pool_rows >> lg_sub;
-  const bool big_pages = p.subpage >= kTileN;
-
-  // Waits are made warp-uniform: the tcgen05.ld/st that follow are warp-collective.
+  const int n = it.n_tiles;
   auto wait_warp = [&](int bar, uint32_t parity, bool cluster) -> bool {
     return __all_sync(0xffffffffu,
                       wait_phase(&sh.bars[bar], parity, sh.abort_flag, p.status, cluster));
   };
 
-  const int n = it.n_tiles;
-  float M = -INFINITY;  // running reference (log2 units), same in both CTAs
-  float l_half = 0.f;   // sum of this half's weights
-  bool ok = true;
-  // own factors (f16, the words sent to the peer) of the last two tiles, in shared
-  // memory (registers are capped at 128 per thread with 14 warps):
-  // [tile%2][half][group 4][row] uint4
-  uint4* eprev = sh.eprev + h * 4 * kRows + r;
-  int32_t pg_next = (big_pages && n > 0) ? __ldg(pages + (it.t_start >> lg_sub)) : 0;
-  for (int i = 0; i <= n; ++i) {
-    // ---------------- front: scores of tile i -> own factors -> peer
-    float e_cur[32];
-    if (i < n) {
-      const int tok0 = it.t_start + i * kTileN;
-      const int32_t pg_tile = pg_next;
-      if (!wait_warp(kBarSFull, i & 1, false)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      {
-        uint32_t sv[32];
-        tmem_ld32(tS, sv);
-        tmem_wait_ld(sv);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) e_cur[c] = __uint_as_float(sv[c]);
-      }
+  float M = -INFINITY;  // running reference (log2 units), same in both CTAs (back warps)
+  float l_half = 0.f;   // sum of this half's weights (back warps)
+  bool ok;
+  if (!back) {
+    {
+      // this warp's 32 rows start at row qw*32 of the tile; the own-factor buffer, first
+      // written after the first scores (which need every warp's q), lends each warp a
+      // 4 KB slice for the transpose
+      const int r_first = qw * 32;
+      const uint16_t* rows0 = p.q + ((int64_t)it.b * qrows + it.qr0 + r_first) * kDqk + d0;
+      const uint32_t tQ = tbase + ((uint32_t)(qw * 32) << 16) + kColQ;
+      const bool q_range = load_q<kFp8, kAtoms>(rows0, it.rows_valid - r_first, h, tQ,
+                                                sh.eprev + warp * 256);
       tc_fence_before();
+      if (q_range) raise_status(p.status, DCP_STATUS_Q_RANGE);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.bars[kBarSFree]);
-      if (big_pages && i + 1 < n) pg_next = __ldg(pages + ((tok0 + kTileN) >> lg_sub));
-      // visible tokens of this row in this half: [tok0 + 32h, row_end), pages valid
-      const int cnt = max(0, min(32, row_end - tok0 - 32 * h));
-      const bool page_ok = !big_pages || (pg_tile >= 0 && pg_tile < pool_pages);
-      // e_cur := 2^(x*sc - m*sc + 14) with x the raw partial score (sc > 0); masked
-      // tokens (past the row's boundary, invalid pages) become -inf, i.e. factor 0
-      uint32_t vis = cnt >= 32 ? 0xFFFFFFFFu : ((1u << cnt) - 1u);
-      if (!page_ok) vis = 0;
-      if (!big_pages && vis) vis = small_page_mask(vis, pages, tok0 + 32 * h, cnt, lg_sub, pool_pages);
-      if (vis != 0xFFFFFFFFu) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) e_cur[c] = ((vis >> c) & 1u) ? e_cur[c] : -INFINITY;
-      }
-      float m4[4] = {e_cur[0], e_cur[1], e_cur[2], e_cur[3]};
-#pragma unroll
-      for (int c = 4; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], e_cur[c]);
-      const float m_cur = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sc;  // -inf: none visible
-      const float bias = m_cur == -INFINITY ? 0.f : kFactorLog2 - m_cur;
-      // x*sc + bias two at a time (packed fp32 FMA), then 2^. on the MUFU unit
-      const float2 sc2 = make_float2(sc, sc), bias2 = make_float2(bias, bias);
-#pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        const float2 y = __ffma2_rn(make_float2(e_cur[c], e_cur[c + 1]), sc2, bias2);
-        e_cur[c] = fast_exp2(y.x);
-        e_cur[c + 1] = fast_exp2(y.y);
-      }
-      // own half maximum for the partner warp (same rows, other half); the arrival is
-      // on the exchange barrier of tile i, which the partner waits for anyway
-      sh.mown[((i % kMOwnBufs) * 2 + h) * kRows + r] = m_cur;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.bars[kBarXFull + (i & 1)]);
-      // send factors (f16 * 2^14) and m to the peer's slot i&1, free since tile i-2
-      const int slot = i & 1;
-      if (i >= 2 && !wait_warp(kBarXFree + slot, ((i >> 1) - 1) & 1, true)) {
-        ok = false;
-        break;
-      }
-      // st.async: each store completes its bytes on the peer's xfull[slot], which the
-      // peer armed with the slot size; no release fence is needed
-      const uint32_t dst = xch_remote + slot * kXchSlotBytes;
-      const uint32_t rbar = xfull_remote + 8 * slot;
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          __half2 hh = __floats2half2_rn(e_cur[8 * g + 2 * e], e_cur[8 * g + 2 * e + 1]);
-          w4[e] = *reinterpret_cast<uint32_t*>(&hh);
-        }
-        st_async_v4(dst + (uint32_t)(((h * 4 + g) * kRows + r) * 16), w4[0], w4[1], w4[2],
-                    w4[3], rbar);
-        eprev[(slot * 8 + g) * kRows] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      }
-      st_async_b32(dst + kXchEBytes + (uint32_t)((h * kRows + r) * 4), __float_as_uint(m_cur),
-                   rbar);
+      if (lane == 0 && !p.hold_q) mbar_arrive(&sh.bars[kBarQFull]);
     }
-    // ---------------- back: finish tile t = i-1 with the peer's factors
-    if (i >= 1) {
-      const int t = i - 1;
-      const int slot = t & 1;
-      // one thread arms this use of the slot with its size (the bytes may already be in)
-      if (tid == 0) {
-        mbar_arrive_expect_tx(&sh.bars[kBarXFull + slot], kXchSlotBytes);
-        if (t == 0) mbar_arrive(&sh.bars[kBarXFull + slot]);  // no P.V before tile 0
-      }
-      if (!wait_warp(kBarXFull + slot, (t >> 1) & 1, true)) {
-        ok = false;
-        break;
-      }
-      const uint8_t* src = sh.xch + slot * kXchSlotBytes;
-      const float* mpeer = reinterpret_cast<const float*>(src + kXchEBytes);
-      const float* mown = sh.mown + (t % kMOwnBufs) * 2 * kRows;
-      // tile bound of the row: max over both halves of m_own + m_peer
-      const float mo0 = mown[r], mo1 = mown[kRows + r];
-      const float mp0 = mpeer[r], mp1 = mpeer[kRows + r];
-      const float ub0 = (mo0 == -INFINITY || mp0 == -INFINITY) ? -INFINITY : mo0 + mp0;
-      const float ub1 = (mo1 == -INFINITY || mp1 == -INFINITY) ? -INFINITY : mo1 + mp1;
-      const float ub = fmaxf(ub0, ub1);
-      const float ub_h = h ? ub1 : ub0;
-      const bool need = ub != -INFINITY && (M == -INFINITY || ub > M + kRaiseAbove);
-      float alpha = 1.f;
-      if (need) {
-        const float m_new = ub - kRefBelow;
-        alpha = M == -INFINITY ? 0.f : fast_exp2(M - m_new);
-        l_half *= alpha;
-        M = m_new;
-      }
-      // P.V(t-1) has completed (its commit was an arrival on this tile's exchange
-      // barrier): the P buffer is free and O is stable
-      tc_fence_after();
-      if (t >= 1 && __any_sync(0xffffffffu, need)) rescale_o(tO, need ? alpha : 1.f);
-      // p = E_own * E_peer * 2^(m_own + m_peer - M); both factors carry 2^14 and are the
-      // f16 words that were exchanged, so the two CTAs form bit-identical weights. 8
-      // tokens per step (two steps per loop body)
-      const float f = ub_h == -INFINITY ? 0.f : fast_exp2(ub_h - M - 2.0f * kFactorLog2);
-      const float2 f2 = make_float2(f, f);
-      float2 lsum2 = make_float2(0.f, 0.f);
-      const uint4* pe_src = reinterpret_cast<const uint4*>(src) + h * 4 * kRows + r;
-      const uint4* own = eprev + slot * 8 * kRows;
-#pragma unroll 2
-      for (int g = 0; g < 4; ++g) {
-        const uint4 a = own[g * kRows], b = pe_src[g * kRows];
-        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          // two weights at a time: the exact f32 product of the two f16 factors, times f
-          const float2 pp = __fmul2_rn(mul_f16x2_f32(aw[e], bw[e]), f2);
-          // l sums the fp32 weights; the P.V contraction uses P rounded to 16 bits
-          lsum2 = __fadd2_rn(lsum2, pp);
-          if (kFp8) {
-            __half2 hh = __floats2half2_rn(pp.x, pp.y);
-            pk[e] = *reinterpret_cast<uint32_t*>(&hh);
-          } else {
-            __nv_bfloat162 hh = __floats2bfloat162_rn(pp.x, pp.y);
-            pk[e] = *reinterpret_cast<uint32_t*>(&hh);
-          }
-        }
-        tmem_st4(tP + 4 * g, pk);
-      }
-      __syncwarp();
-      // done with the peer's slot: its values are in registers already
-      if (lane == 0) mbar_arrive_remote_relaxed(xfree_remote + 8 * slot);
-      l_half += lsum2.x + lsum2.y;
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.bars[kBarPFull]);
-    }
+    cluster_wait();  // the peer's barriers are initialised before this warp's first send
+    const int L = row_ok ? p.row_len[(int64_t)it.k * R + (int64_t)it.b * p.qlen + j] : 0;
+    const int row_end = min(L, it.t_end);  // tokens at or past it are invisible to this row
+    const float sc = p.softmax_scale * kv_scale * kLog2e;
+    ok = run_front<kFp8, kAtoms>(p, sh, it, tbase, lane, qw, h, r, row_end, sc);
+  } else {
+    ok = run_back<kFp8>(p, sh, it, tbase, cta, lane, warp, qw, h, r, M, l_half);
   }
 
-  // epilogue: both halves' l, then this warp's 128 O columns of its rows
+  // epilogue: the back warps combine both halves' l into the row's output scale; every
+  // softmax warp then stores 64 O columns of its rows
   const bool have_o =
       __all_sync(0xffffffffu, ok) && n > 0 && wait_warp(kBarODone, (n - 1) & 1, false);
   tc_fence_after();
-  sh.lcomb[h * kRows + r] = l_half;
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&sh.bars[kBarLComb]);
-  const bool paired = wait_warp(kBarLComb, 0, false);
-  const float l_run = l_half + sh.lcomb[(h ^ 1) * kRows + r];
+  float inv = 0.f, l_run = 0.f;
+  if (back) {
+    sh.lcomb[h * kRows + r] = l_half;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.bars[kBarLComb]);
+    const bool paired = wait_warp(kBarLComb, 0, false);
+    l_run = l_half + sh.lcomb[(h ^ 1) * kRows + r];
+    inv = (paired && l_run > 0.f) ? kv_scale / l_run : 0.f;
+    if (h == 0) sh.einv[r] = inv;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.bars[kBarEpi]);
+  } else if (wait_warp(kBarEpi, 0, false)) {
+    inv = sh.einv[r];
+  }
+  const int col_w = 128 * h + (back ? 64 : 0);  // the warp's columns within the CTA's 256
+  const uint32_t tO = tbase + ((uint32_t)(qw * 32) << 16) + kColO + col_w;
   const int64_t rh = (int64_t)it.b * qrows + qr;
   const int64_t base = ((int64_t)it.k * p.num_splits + it.s) * ((int64_t)R * p.H) + rh;
-  const float inv = (paired && l_run > 0.f) ? kv_scale / l_run : 0.f;
-  // the warp's first row; every MMA has completed (or none ran), so the KV stages are
-  // free and lend each warp a 4 KB slice for the transpose
+  // every MMA has completed (or none ran), so the KV stages are free and lend each warp
+  // a 4 KB slice for the transpose
   uint4* slice = reinterpret_cast<uint4*>(sh.stages) + warp * 256;
+  const bool lse_owner = back && row_ok && cta == 0 && h == 0;
   if (p.send != nullptr) {
     // packed epilogue
     const int Hg = p.H / p.G;
     store_o_packed(tO, have_o, it.rows_valid - qw * 32, inv, slice,
                    p.send + (int64_t)it.k * p.G * p.send_cw, p.send_cw, p.H, Hg,
-                   it.qr0 + qw * 32, (int64_t)it.b * p.qlen, 256 * cta + 128 * h);
-    if (row_ok && cta == 0 && h == 0) {
+                   it.qr0 + qw * 32, (int64_t)it.b * p.qlen, 256 * cta + col_w);
+    if (lse_owner) {
       // the LSE words (low 16 bits, then high), as one 32-bit store
       const float lse = l_run > 0.f ? (M + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       const int hh = qr - j * p.H, dd = hh / Hg;
@@ -1016,9 +1061,9 @@ __device__ __forceinline__ void run_softmax(const Params& p, const Shared& sh, c
     return;
   }
   const int64_t base0 = base - r + qw * 32;
-  store_o(tO, have_o, it.rows_valid - qw * 32, inv, p.part_o + base0 * kDv + 256 * cta + 128 * h,
-          slice);
-  if (row_ok && cta == 0 && h == 0) {
+  store_o(tO, have_o, it.rows_valid - qw * 32, inv,
+          p.part_o + base0 * kDv + 256 * cta + col_w, slice);
+  if (lse_owner) {
     p.part_m[base] = l_run > 0.f ? M : -INFINITY;
     p.part_l[base] = l_run;
     if (it.s == 0) {
@@ -1140,17 +1185,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&sh.bars[kBarKvEmpty + i], 2);
     }
     mbar_init(&sh.bars[kBarSFull], 1);
-    mbar_init(&sh.bars[kBarSFree], kSoftWarps);
-    mbar_init(&sh.bars[kBarPFull], kSoftWarps);
+    mbar_init(&sh.bars[kBarSFree], kFrontWarps);
+    mbar_init(&sh.bars[kBarPFull], kBackWarps);
     mbar_init(&sh.bars[kBarODone], 1);
-    mbar_init(&sh.bars[kBarQFull], kSoftWarps);
+    mbar_init(&sh.bars[kBarQFull], kFrontWarps);
     for (int i = 0; i < kXchSlots; ++i) {
-      // armed by one local thread with the slot's bytes; the 8 local warps arrive, and
-      // the completion of the previous tile's P.V (tile 0: the arming thread again)
-      mbar_init(&sh.bars[kBarXFull + i], 2 + kSoftWarps);
-      mbar_init(&sh.bars[kBarXFree + i], kSoftWarps);
+      // armed by one back-warp thread with the slot's bytes; the 8 front warps arrive,
+      // and the completion of the previous tile's P.V (tile 0: the arming thread again)
+      mbar_init(&sh.bars[kBarXFull + i], 2 + kFrontWarps);
+      mbar_init(&sh.bars[kBarXFree + i], kBackWarps);
+      mbar_init(&sh.bars[kBarEFree + i], kBackWarps);
     }
-    mbar_init(&sh.bars[kBarLComb], kSoftWarps);
+    mbar_init(&sh.bars[kBarLComb], kBackWarps);
+    mbar_init(&sh.bars[kBarEpi], kBackWarps);
     mbar_init(&sh.bars[kBarDrainS], 1);
     mbar_init(&sh.bars[kBarDrainP], 1);
     *sh.abort_flag = 0;
@@ -1165,10 +1212,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   // this CTA's barriers are ready for the peer. A thread waits for the peer's only where
-  // it first needs them: the softmax warps before their first send (their q load runs
+  // it first needs them: the front warps before their first send (their q load runs
   // meanwhile), every other warp here
   cluster_arrive();
-  if (warp >= kSoftWarps) cluster_wait();
+  if (warp >= kFrontWarps) cluster_wait();
   tc_fence_after();
   const uint32_t tbase = __shfl_sync(0xffffffffu, *sh.tmem_slot, 0);
 
@@ -1270,15 +1317,27 @@ int partial_concurrent_items() {
   if (cached[dev] > 0) return cached[dev];
   // both instantiations take the same threads and shared memory
   auto kern = partial_tc_kernel<true>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-      cudaSuccess)
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) {
+    fail(DCP_ERR_CUDA, "partial kernel shared-memory attribute: %s", cudaGetErrorString(e));
     return -1;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * 4096);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;  // cluster shape from the kernel's own attribute
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return -1;
+  e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+  if (e != cudaSuccess || n < 1) {
+    cudaFuncAttributes fa = {};
+    cudaFuncGetAttributes(&fa, kern);
+    fail(DCP_ERR_CUDA,
+         "partial kernel occupancy: %s, %d clusters (%d threads of %d registers, at most %d "
+         "threads per block; %zu bytes of shared memory)",
+         cudaGetErrorString(e), n, kThreads, fa.numRegs, fa.maxThreadsPerBlock, kSmemBytes);
+    return -1;
+  }
   cached[dev] = n;
   return n;
 }

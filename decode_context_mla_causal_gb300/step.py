@@ -49,7 +49,7 @@ def concurrent_items() -> int:
     """Work items the partial kernel runs at once on the current device."""
     n = B.dcp_mla_concurrent_items()
     if n < 1:
-        raise RuntimeError("no CUDA device to size the split plan for")
+        raise RuntimeError("no CUDA device to size the split plan for: " + B.dcp_last_error())
     return n
 
 

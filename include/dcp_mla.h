@@ -171,7 +171,8 @@ dcp_status dcp_mla_metadata(const dcp_mla_dims* dims, const int32_t* seq_lens,
                             int32_t* split_end, uint32_t* status, dcp_stream_t stream);
 
 /* Work items (clusters of two CTAs) of dcp_mla_partial that the current device
- * runs at once; -1 if there is no device or the query fails. Host only. */
+ * runs at once; -1 if there is no device or the query fails (dcp_last_error()
+ * then says why). Host only. */
 int32_t dcp_mla_concurrent_items(void);
 
 /*
