@@ -1313,7 +1313,12 @@ size_t partial_workspace_bytes(const dcp_mla_dims& d, int num_ranks) {
 int partial_concurrent_items() {
   static int cached[64] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  const cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess || dev < 0 || dev >= 64) {
+    fail(DCP_ERR_CUDA, "no usable CUDA device: %s",
+         de != cudaSuccess ? cudaGetErrorString(de) : "device index out of range");
+    return -1;
+  }
   if (cached[dev] > 0) return cached[dev];
   // both instantiations take the same threads and shared memory
   auto kern = partial_tc_kernel<true>;

@@ -93,6 +93,7 @@ def test_concurrent_items_without_a_device(dm):
         assert dm.dcp_mla_concurrent_items() >= 1
     else:
         assert dm.dcp_mla_concurrent_items() == -1
+        assert "CUDA device" in dm.dcp_last_error()  # the failure says why
 
 
 def test_rank_range_checked(dm):
